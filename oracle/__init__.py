@@ -1,0 +1,17 @@
+"""CPU oracle for block top-k (centroid-scored) decode attention.
+
+TEST INFRASTRUCTURE, not part of the product.  Only the test suite, the smoke check in
+``__graft_entry__`` and the CPU-baseline leg of ``bench.py`` may import or run it.  It
+shares no code with the CUDA library: it reads the same seeded host inputs and nothing
+else, and it never reads anything the CUDA path computed.
+
+See ``oracle.blocktopk`` for the method and the passages each function follows.
+"""
+from .blocktopk import (BLOCK, round_to_bf16, block_centroid, centroids, group_scores,
+                        select_blocks, attend, row_tokens, decode_rows, blocktopk_decode,
+                        dense_decode, decode_bytes, dense_kv_bytes_per_step,
+                        sparse_kv_tokens)
+
+__all__ = ["BLOCK", "round_to_bf16", "block_centroid", "centroids", "group_scores",
+           "select_blocks", "attend", "row_tokens", "decode_rows", "blocktopk_decode",
+           "dense_decode", "decode_bytes", "dense_kv_bytes_per_step", "sparse_kv_tokens"]
