@@ -418,4 +418,6 @@ def test_planted_mistake_is_caught(name, monkeypatch):
             pin()
         except AssertionError:
             failed.append(pin.__name__)
+        except Exception:          # a crash elsewhere is not what we look for
+            pass
     assert failed, f"no pin caught the planted mistake {name}"
