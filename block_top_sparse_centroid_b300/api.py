@@ -1,0 +1,274 @@
+"""Python binding of libkin: argument marshalling over torch tensors, nothing else.
+
+Every step of the path runs in the CUDA library; this module only checks tensor
+shapes / dtypes / devices, allocates outputs and the workspace through torch when the
+caller does not pass them, and forwards raw pointers and the current stream to the C ABI.
+
+The method (block top-k decode attention over a paged KV cache, blocks of 16 tokens
+scored by their mean key vectors, summed over the GQA group) follows the Pith review of
+"Kinetics: Rethinking Test-Time Scaling Laws", section "What carries the argument", and
+the Kinetics README, section "Benchmark Block TopK Attention throughput".
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+
+BLOCK = 16
+_DTYPES = {torch.float32: L.KIN_F32, torch.bfloat16: L.KIN_BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, shape, dtype, device) -> None:
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+@dataclasses.dataclass
+class PagedKVCache:
+    """K and V pages of one attention layer: [num_pages, num_kv_heads, 16, head_dim]."""
+
+    k_pages: torch.Tensor
+    v_pages: torch.Tensor
+
+    def __post_init__(self):
+        k, v = self.k_pages, self.v_pages
+        if k.dim() != 4 or k.shape[2] != BLOCK:
+            raise ValueError("k_pages must be [num_pages, num_kv_heads, 16, head_dim]")
+        if v.shape != k.shape or v.dtype != k.dtype or v.device != k.device:
+            raise ValueError("v_pages must match k_pages in shape, dtype and device")
+        if k.dtype not in _DTYPES:
+            raise ValueError(f"unsupported dtype {k.dtype}")
+        if not (k.is_contiguous() and v.is_contiguous()):
+            raise ValueError("pages must be contiguous")
+
+    @property
+    def device(self):
+        return self.k_pages.device
+
+    @property
+    def dtype(self):
+        return self.k_pages.dtype
+
+    @property
+    def num_pages(self) -> int:
+        return int(self.k_pages.shape[0])
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.k_pages.shape[1])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.k_pages.shape[3])
+
+    def c_struct(self) -> L.KvCache:
+        return L.KvCache(_DTYPES[self.dtype], self.num_kv_heads, self.head_dim, BLOCK,
+                         self.num_pages, self.k_pages.data_ptr(), self.v_pages.data_ptr())
+
+
+def _shape_args(cache: PagedKVCache, batch: int, num_q_heads: int, max_blocks: int,
+                top_k: int) -> L.DecodeArgs:
+    a = L.DecodeArgs()
+    a.batch, a.num_q_heads, a.max_blocks, a.top_k = batch, num_q_heads, max_blocks, top_k
+    a.sm_scale = 1.0
+    return a
+
+
+def workspace_size(cache: PagedKVCache, batch: int, num_q_heads: int, max_blocks: int,
+                   top_k: int = 1, dense: bool = False) -> int:
+    """Bytes of workspace one decode call needs (kin_workspace_size)."""
+    lib = L.load()
+    c = cache.c_struct()
+    a = _shape_args(cache, batch, num_q_heads, max_blocks, top_k)
+    n = ctypes.c_size_t(0)
+    L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a),
+                                   L.MODE_DENSE if dense else L.MODE_BLOCKTOPK, ctypes.byref(n)),
+            "kin_workspace_size")
+    return int(n.value)
+
+
+class Workspace:
+    """A zero-filled device scratch buffer that grows on demand (one per stream)."""
+
+    def __init__(self, device):
+        self.device = torch.device(device)
+        self.buf = torch.zeros(0, dtype=torch.uint8, device=self.device)
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_default_ws = {}
+
+
+def _workspace(device, nbytes: int, workspace: Optional[Workspace]) -> torch.Tensor:
+    if workspace is None:
+        key = (device.type, device.index)
+        workspace = _default_ws.get(key)
+        if workspace is None:
+            workspace = _default_ws[key] = Workspace(device)
+    return workspace.get(nbytes)
+
+
+def _err_ptr(err_flag: Optional[torch.Tensor], device):
+    if err_flag is None:
+        return None
+    _need(err_flag, "err_flag", (1,), torch.int32, device)
+    return _ptr(err_flag)
+
+
+def centroids_build(cache: PagedKVCache, centroids: Optional[torch.Tensor] = None,
+                    page_ids: Optional[torch.Tensor] = None,
+                    err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Mean key of every listed page (all pages when page_ids is None): kin_centroids_build."""
+    lib = L.load()
+    dev = cache.device
+    shape = (cache.num_pages, cache.num_kv_heads, cache.head_dim)
+    if centroids is None:
+        centroids = torch.empty(shape, dtype=cache.dtype, device=dev)
+    _need(centroids, "centroids", shape, cache.dtype, dev)
+    n = cache.num_pages
+    if page_ids is not None:
+        if page_ids.dim() != 1:
+            raise ValueError("page_ids must be 1-D")
+        _need(page_ids, "page_ids", (page_ids.numel(),), torch.int32, dev)
+        n = page_ids.numel()
+    c = cache.c_struct()
+    L.check(lib.kin_centroids_build(ctypes.byref(c), _ptr(page_ids), n, _ptr(centroids),
+                                    _err_ptr(err_flag, dev), _stream(stream, dev)),
+            "kin_centroids_build")
+    return centroids
+
+
+def centroids_append(cache: PagedKVCache, page_ids: torch.Tensor, centroids: torch.Tensor,
+                     err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Mean key of pages a decode step just completed: kin_centroids_append."""
+    lib = L.load()
+    dev = cache.device
+    _need(centroids, "centroids", (cache.num_pages, cache.num_kv_heads, cache.head_dim),
+          cache.dtype, dev)
+    if page_ids.dim() != 1:
+        raise ValueError("page_ids must be 1-D")
+    _need(page_ids, "page_ids", (page_ids.numel(),), torch.int32, dev)
+    c = cache.c_struct()
+    L.check(lib.kin_centroids_append(ctypes.byref(c), _ptr(page_ids), page_ids.numel(),
+                                     _ptr(centroids), _err_ptr(err_flag, dev),
+                                     _stream(stream, dev)),
+            "kin_centroids_append")
+    return centroids
+
+
+def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, top_k,
+            centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream, events=None):
+    lib = L.load()
+    dev = cache.device
+    if q.dim() != 3:
+        raise ValueError("q must be [batch, num_q_heads, head_dim]")
+    B, Hq, d = (int(x) for x in q.shape)
+    H = cache.num_kv_heads
+    _need(q, "q", (B, Hq, cache.head_dim), cache.dtype, dev)
+    if block_table.dim() != 2:
+        raise ValueError("block_table must be [batch, max_blocks]")
+    maxb = int(block_table.shape[1])
+    _need(block_table, "block_table", (B, maxb), torch.int32, dev)
+    _need(seq_lens, "seq_lens", (B,), torch.int32, dev)
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", (B, Hq, d), cache.dtype, dev)
+    if lse is not None:
+        _need(lse, "lse", (B, Hq), torch.float32, dev)
+    if mode == L.MODE_BLOCKTOPK:
+        _need(centroids, "centroids", (cache.num_pages, H, d), cache.dtype, dev)
+        if sel_blocks is not None:
+            _need(sel_blocks, "sel_blocks", (B, H, top_k), torch.int32, dev)
+        if scores is not None:
+            _need(scores, "scores", (B, H, maxb), torch.float32, dev)
+    a = L.DecodeArgs()
+    a.batch, a.num_q_heads, a.max_blocks, a.top_k = B, Hq, maxb, int(top_k)
+    a.sm_scale = float(sm_scale)
+    a.q, a.block_table, a.seq_lens = q.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr()
+    a.centroids = centroids.data_ptr() if (centroids is not None and mode == 0) else None
+    a.out = out.data_ptr()
+    a.lse = None if lse is None else lse.data_ptr()
+    a.sel_blocks = None if (sel_blocks is None or mode != 0) else sel_blocks.data_ptr()
+    a.scores = None if (scores is None or mode != 0) else scores.data_ptr()
+    c = cache.c_struct()
+    need = ctypes.c_size_t(0)
+    L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a), mode, ctypes.byref(need)),
+            "kin_workspace_size")
+    ws = _workspace(dev, int(need.value), workspace)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+    a.err_flag = None if err_flag is None else _err_ptr(err_flag, dev).value
+    if events is not None:
+        handles = (ctypes.c_void_p * 4)(*[_event_handle(e, stream, dev) for e in events])
+        L.check(lib.kin_decode_timed(ctypes.byref(c), ctypes.byref(a), mode, handles,
+                                     _stream(stream, dev)), "kin_decode_timed")
+        return out
+    fn = lib.kin_blocktopk_decode if mode == L.MODE_BLOCKTOPK else lib.kin_dense_decode
+    L.check(fn(ctypes.byref(c), ctypes.byref(a), _stream(stream, dev)),
+            "kin_blocktopk_decode" if mode == L.MODE_BLOCKTOPK else "kin_dense_decode")
+    return out
+
+
+def _event_handle(ev: "torch.cuda.Event", stream, dev) -> int:
+    """Raw cudaEvent_t of a torch event (torch creates the event on its first record)."""
+    if ev.cuda_event == 0:
+        ev.record(stream if stream is not None else torch.cuda.current_stream(dev))
+    return ev.cuda_event
+
+
+def blocktopk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                     seq_lens: torch.Tensor, centroids: torch.Tensor, top_k: int,
+                     sm_scale: float, out: Optional[torch.Tensor] = None,
+                     lse: Optional[torch.Tensor] = None,
+                     sel_blocks: Optional[torch.Tensor] = None,
+                     scores: Optional[torch.Tensor] = None,
+                     workspace: Optional[Workspace] = None,
+                     err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One block top-k decode step (score, select, sparse attention): kin_blocktopk_decode."""
+    return _decode(L.MODE_BLOCKTOPK, cache, q, block_table, seq_lens, sm_scale, top_k,
+                   centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream)
+
+
+def decode_timed(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, sm_scale: float, events, dense: bool = False,
+                 centroids: Optional[torch.Tensor] = None, top_k: int = 1,
+                 out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
+                 err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """One decode step that also records 4 torch.cuda.Events around its kernels
+    (before scoring, after scoring, after selection, after attention): kin_decode_timed."""
+    mode = L.MODE_DENSE if dense else L.MODE_BLOCKTOPK
+    return _decode(mode, cache, q, block_table, seq_lens, sm_scale, top_k, centroids, out,
+                   None, None, None, workspace, err_flag, stream, events=list(events))
+
+
+def dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                 seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
+                 lse: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
+                 err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Dense paged decode over every block (the comparison baseline): kin_dense_decode."""
+    return _decode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, None, out,
+                   lse, None, None, workspace, err_flag, stream)

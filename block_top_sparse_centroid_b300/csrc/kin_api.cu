@@ -1,0 +1,396 @@
+// C-ABI entry points of libkin: argument validation, workspace layout, split planning,
+// TMA descriptor encoding and kernel launches.  Every call validates on the host first
+// and enqueues nothing when it returns an error.  No call allocates or synchronises.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "kin_common.cuh"
+#include "kin_internal.h"
+
+namespace kin {
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+kin_status fail(kin_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kin_status ok() {
+  g_last_error[0] = '\0';
+  return KIN_OK;
+}
+
+kin_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(KIN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Split planning is a pure function of the shapes (never of the device), so the
+// workspace size and the launch always agree.  It targets about two waves of
+// attention CTAs over the 148 SMs of a B300 at three resident CTAs per SM.
+constexpr int kPlanSMs = 148;
+constexpr int kPlanCtasPerSM = 3;
+constexpr int kMaxItemsPerSplit = 256;
+constexpr int kMaxBlocksLimit = 16384;
+
+struct Plan {
+  int rows, group, max_items, items_per_split, max_splits, score_chunk;
+};
+
+Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
+  Plan pl{};
+  pl.rows = a->batch * c->num_kv_heads;
+  pl.group = a->num_q_heads / c->num_kv_heads;
+  pl.max_items = mode == 0 ? (a->top_k < a->max_blocks ? a->top_k : a->max_blocks) : a->max_blocks;
+  const int warps = attention_warps();
+  const int target = kPlanSMs * kPlanCtasPerSM * 2;
+  int splits = (target + pl.rows - 1) / pl.rows;
+  const int max_useful = (pl.max_items + 2 * warps - 1) / (2 * warps);  // >= 2 blocks per warp
+  if (splits > max_useful) splits = max_useful;
+  if (splits < 1) splits = 1;
+  int ips = (pl.max_items + splits - 1) / splits;
+  ips = (ips + warps - 1) / warps * warps;
+  if (ips > kMaxItemsPerSplit) ips = kMaxItemsPerSplit;
+  pl.items_per_split = ips;
+  pl.max_splits = (pl.max_items + ips - 1) / ips;
+  // Score chunk: about 8 CTAs per SM over all candidate blocks, 64..1024 per CTA.
+  const long long cand = static_cast<long long>(pl.rows) * a->max_blocks;
+  long long chunk = (cand + kPlanSMs * 8 - 1) / (kPlanSMs * 8);
+  chunk = (chunk + 63) / 64 * 64;
+  if (chunk < 64) chunk = 64;
+  if (chunk > 1024) chunk = 1024;
+  pl.score_chunk = static_cast<int>(chunk);
+  return pl;
+}
+
+struct Layout {
+  size_t counters, part_ml, part_o, scores, sel, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &pl, int mode) {
+  Layout L{};
+  size_t off = 0;
+  L.counters = off;
+  off = align256(off + sizeof(int32_t) * pl.rows);
+  L.part_ml = off;
+  off = align256(off + sizeof(float) * 2 * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group);
+  L.part_o = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group *
+                           c->head_dim);
+  L.scores = off;
+  if (mode == 0) off = align256(off + sizeof(float) * static_cast<size_t>(pl.rows) * a->max_blocks);
+  L.sel = off;
+  if (mode == 0) off = align256(off + sizeof(int32_t) * static_cast<size_t>(pl.rows) * a->top_k);
+  L.total = off;
+  return L;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kin_status check_cache_shape(const kin_kv_cache *c) {
+  if (c == nullptr) return fail(KIN_ERR_INVALID_ARG, "cache is NULL");
+  if (c->dtype != KIN_F32 && c->dtype != KIN_BF16)
+    return fail(KIN_ERR_UNSUPPORTED, "dtype %d is not f32 (0) or bf16 (1)", static_cast<int>(c->dtype));
+  if (c->page_size != kBlock)
+    return fail(KIN_ERR_UNSUPPORTED, "page_size %d: only 16-token pages are supported", c->page_size);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(KIN_ERR_UNSUPPORTED, "head_dim %d: only 64 and 128 are supported", c->head_dim);
+  if (c->num_kv_heads < 1) return fail(KIN_ERR_INVALID_ARG, "num_kv_heads %d < 1", c->num_kv_heads);
+  if (c->num_pages < 1) return fail(KIN_ERR_INVALID_ARG, "num_pages %lld < 1", (long long)c->num_pages);
+  if (c->num_pages * c->num_kv_heads * kBlock >= (1LL << 31))
+    return fail(KIN_ERR_UNSUPPORTED, "num_pages * num_kv_heads * 16 must be below 2^31");
+  return ok();
+}
+
+kin_status check_cache(const kin_kv_cache *c) {
+  kin_status s = check_cache_shape(c);
+  if (s != KIN_OK) return s;
+  if (c->k_pages == nullptr || c->v_pages == nullptr)
+    return fail(KIN_ERR_INVALID_ARG, "k_pages / v_pages is NULL");
+  if (!aligned16(c->k_pages) || !aligned16(c->v_pages))
+    return fail(KIN_ERR_INVALID_ARG, "k_pages / v_pages must be 16-byte aligned");
+  return ok();
+}
+
+kin_status check_args(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
+  if (a == nullptr) return fail(KIN_ERR_INVALID_ARG, "args is NULL");
+  if (a->batch < 1) return fail(KIN_ERR_INVALID_ARG, "batch %d < 1", a->batch);
+  if (a->num_q_heads < 1 || a->num_q_heads % c->num_kv_heads != 0)
+    return fail(KIN_ERR_INVALID_ARG, "num_q_heads %d is not a positive multiple of num_kv_heads %d",
+                a->num_q_heads, c->num_kv_heads);
+  const int G = a->num_q_heads / c->num_kv_heads;
+  if (G > 16) return fail(KIN_ERR_UNSUPPORTED, "group size %d > 16", G);
+  if (a->max_blocks < 1 || a->max_blocks > kMaxBlocksLimit)
+    return fail(KIN_ERR_UNSUPPORTED, "max_blocks %d outside 1..%d", a->max_blocks, kMaxBlocksLimit);
+  if (mode == 0 && a->top_k < 1) return fail(KIN_ERR_INVALID_ARG, "top_k %d < 1", a->top_k);
+  if (!(a->sm_scale > 0.f) || a->sm_scale == INFINITY)
+    return fail(KIN_ERR_INVALID_ARG, "sm_scale must be a positive finite number");
+  if (a->q == nullptr || a->block_table == nullptr || a->seq_lens == nullptr || a->out == nullptr)
+    return fail(KIN_ERR_INVALID_ARG, "q / block_table / seq_lens / out must not be NULL");
+  if (!aligned16(a->q)) return fail(KIN_ERR_INVALID_ARG, "q must be 16-byte aligned");
+  if (mode == 0) {
+    if (a->centroids == nullptr) return fail(KIN_ERR_INVALID_ARG, "centroids must not be NULL");
+    if (!aligned16(a->centroids)) return fail(KIN_ERR_INVALID_ARG, "centroids must be 16-byte aligned");
+  }
+  return ok();
+}
+
+kin_status check_workspace(const kin_decode_args *a, const Layout &L) {
+  if (a->workspace == nullptr)
+    return fail(KIN_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", L.total);
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail(KIN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (a->workspace_bytes < L.total)
+    return fail(KIN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", a->workspace_bytes, L.total);
+  return ok();
+}
+
+// --- TMA descriptors -----------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// View the page pool as a 2-D bf16 tensor [P*H*16 rows, d columns] and move 64-column
+// by 16-row boxes (one page of one head) with the 128-byte swizzle.
+kin_status encode_page_map(CUtensorMap *map, const kin_kv_cache *c, const void *base) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return fail(KIN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->head_dim),
+                              static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * kBlock};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->head_dim) * 2};
+  const cuuint32_t box[2] = {64, kBlock};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KIN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return KIN_OK;
+}
+
+// Make the device that holds `ptr` current (the caller's framework may have another
+// device current in its own runtime instance).
+kin_status use_device_of(const void *ptr) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(KIN_ERR_INVALID_ARG, "cache pages are not device memory");
+  int cur = -1;
+  e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != attr.device) {
+    e = cudaSetDevice(attr.device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  }
+  return KIN_OK;
+}
+
+kin_status record(void *const *events, int i, cudaStream_t stream) {
+  if (events == nullptr) return KIN_OK;
+  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+  return KIN_OK;
+}
+
+kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
+                      cudaStream_t stream, void *const *events = nullptr) {
+  kin_status s = check_cache(c);
+  if (s != KIN_OK) return s;
+  s = check_args(c, a, mode);
+  if (s != KIN_OK) return s;
+  const Plan pl = make_plan(c, a, mode);
+  const Layout L = make_layout(c, a, pl, mode);
+  s = check_workspace(a, L);
+  if (s != KIN_OK) return s;
+  if (events != nullptr && (events[0] == nullptr || events[1] == nullptr ||
+                            events[2] == nullptr || events[3] == nullptr))
+    return fail(KIN_ERR_INVALID_ARG, "events must hold 4 created CUDA events");
+  s = use_device_of(c->k_pages);
+  if (s != KIN_OK) return s;
+  uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+  if ((s = record(events, 0, stream)) != KIN_OK) return s;
+
+  const int32_t *sel = nullptr;
+  if (mode == 0) {
+    ScoreParams sp{};
+    sp.q = a->q;
+    sp.centroids = a->centroids;
+    sp.block_table = a->block_table;
+    sp.seq_lens = a->seq_lens;
+    sp.scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
+    sp.sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
+    sp.err = a->err_flag;
+    sp.num_pages = c->num_pages;
+    sp.batch = a->batch;
+    sp.num_kv_heads = c->num_kv_heads;
+    sp.group = pl.group;
+    sp.max_blocks = a->max_blocks;
+    sp.top_k = a->top_k;
+    sp.chunk = pl.score_chunk;
+    cudaError_t e = launch_score(c->dtype, c->head_dim, sp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "score kernel launch");
+    if ((s = record(events, 1, stream)) != KIN_OK) return s;
+    e = launch_select(sp, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "select kernel launch");
+    if ((s = record(events, 2, stream)) != KIN_OK) return s;
+    sel = sp.sel;
+  } else {
+    if ((s = record(events, 1, stream)) != KIN_OK) return s;
+    if ((s = record(events, 2, stream)) != KIN_OK) return s;
+  }
+
+  AttnParams ap{};
+  ap.q = a->q;
+  ap.k_pages = c->k_pages;
+  ap.v_pages = c->v_pages;
+  ap.block_table = a->block_table;
+  ap.seq_lens = a->seq_lens;
+  ap.sel = sel;
+  ap.out = a->out;
+  ap.lse = a->lse;
+  ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  ap.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
+  ap.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  ap.err = a->err_flag;
+  ap.num_pages = c->num_pages;
+  ap.batch = a->batch;
+  ap.num_kv_heads = c->num_kv_heads;
+  ap.group = pl.group;
+  ap.max_blocks = a->max_blocks;
+  ap.sel_stride = mode == 0 ? a->top_k : 0;
+  ap.items_per_split = pl.items_per_split;
+  ap.max_splits = pl.max_splits;
+  ap.sm_scale = a->sm_scale;
+  CUtensorMap kmap, vmap;
+  std::memset(&kmap, 0, sizeof(kmap));
+  std::memset(&vmap, 0, sizeof(vmap));
+  if (c->dtype == KIN_BF16) {
+    s = encode_page_map(&kmap, c, c->k_pages);
+    if (s != KIN_OK) return s;
+    s = encode_page_map(&vmap, c, c->v_pages);
+    if (s != KIN_OK) return s;
+  }
+  cudaError_t e = launch_attention(c->dtype, c->head_dim, ap, &kmap, &vmap, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  if ((s = record(events, 3, stream)) != KIN_OK) return s;
+  return ok();
+}
+
+kin_status run_centroids(const kin_kv_cache *c, const int32_t *page_ids, int64_t n,
+                         void *centroids, int32_t *err, cudaStream_t stream) {
+  kin_status s = check_cache(c);
+  if (s != KIN_OK) return s;
+  if (n < 0) return fail(KIN_ERR_INVALID_ARG, "n %lld < 0", (long long)n);
+  if (centroids == nullptr) return fail(KIN_ERR_INVALID_ARG, "centroids is NULL");
+  if (!aligned16(centroids)) return fail(KIN_ERR_INVALID_ARG, "centroids must be 16-byte aligned");
+  if (page_ids == nullptr && n != c->num_pages)
+    return fail(KIN_ERR_INVALID_ARG, "page_ids is NULL but n (%lld) != num_pages (%lld)",
+                (long long)n, (long long)c->num_pages);
+  if (n == 0) return ok();
+  s = use_device_of(c->k_pages);
+  if (s != KIN_OK) return s;
+  cudaError_t e = launch_centroids(c->dtype, c->head_dim, c->num_kv_heads, c->k_pages,
+                                   c->num_pages, page_ids, n, centroids, err, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "centroid kernel launch");
+  return ok();
+}
+
+}  // namespace
+}  // namespace kin
+
+extern "C" {
+
+const char *kin_status_str(kin_status s) {
+  switch (s) {
+    case KIN_OK: return "KIN_OK";
+    case KIN_ERR_INVALID_ARG: return "KIN_ERR_INVALID_ARG";
+    case KIN_ERR_UNSUPPORTED: return "KIN_ERR_UNSUPPORTED";
+    case KIN_ERR_WORKSPACE: return "KIN_ERR_WORKSPACE";
+    case KIN_ERR_CUDA: return "KIN_ERR_CUDA";
+  }
+  return "KIN_ERR_UNKNOWN";
+}
+
+const char *kin_last_error(void) { return kin::g_last_error; }
+
+kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *args, int32_t mode,
+                              size_t *bytes) {
+  using namespace kin;
+  if (bytes == nullptr) return fail(KIN_ERR_INVALID_ARG, "bytes is NULL");
+  if (mode != 0 && mode != 1) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0 or 1", mode);
+  kin_status s = check_cache_shape(cache);
+  if (s != KIN_OK) return s;
+  if (args == nullptr) return fail(KIN_ERR_INVALID_ARG, "args is NULL");
+  if (args->batch < 1 || args->num_q_heads < 1 || args->max_blocks < 1 ||
+      args->max_blocks > kMaxBlocksLimit || args->num_q_heads % cache->num_kv_heads != 0 ||
+      args->num_q_heads / cache->num_kv_heads > 16 || (mode == 0 && args->top_k < 1))
+    return fail(KIN_ERR_INVALID_ARG, "bad shapes for workspace sizing");
+  const Plan pl = make_plan(cache, args, mode);
+  *bytes = make_layout(cache, args, pl, mode).total;
+  return ok();
+}
+
+kin_status kin_workspace_init(void *workspace, size_t bytes, kin_stream_t stream) {
+  using namespace kin;
+  if (workspace == nullptr) return fail(KIN_ERR_INVALID_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return ok();
+}
+
+kin_status kin_centroids_build(const kin_kv_cache *cache, const int32_t *page_ids, int64_t n,
+                               void *centroids, int32_t *err_flag, kin_stream_t stream) {
+  return kin::run_centroids(cache, page_ids, n, centroids, err_flag,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+kin_status kin_centroids_append(const kin_kv_cache *cache, const int32_t *page_ids, int32_t n,
+                                void *centroids, int32_t *err_flag, kin_stream_t stream) {
+  using namespace kin;
+  if (n > 0 && page_ids == nullptr) return fail(KIN_ERR_INVALID_ARG, "page_ids is NULL");
+  return kin::run_centroids(cache, page_ids, n, centroids, err_flag,
+                            reinterpret_cast<cudaStream_t>(stream));
+}
+
+kin_status kin_blocktopk_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                                kin_stream_t stream) {
+  return kin::run_decode(cache, args, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                            kin_stream_t stream) {
+  return kin::run_decode(cache, args, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+kin_status kin_decode_timed(const kin_kv_cache *cache, const kin_decode_args *args, int32_t mode,
+                            void *const *events, kin_stream_t stream) {
+  using namespace kin;
+  if (mode != 0 && mode != 1) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0 or 1", mode);
+  if (events == nullptr) return fail(KIN_ERR_INVALID_ARG, "events is NULL");
+  return kin::run_decode(cache, args, mode, reinterpret_cast<cudaStream_t>(stream), events);
+}
+
+}  // extern "C"

@@ -1,0 +1,61 @@
+// Host-side declarations shared by the translation units of libkin.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kin.h"
+
+namespace kin {
+
+// Centroid (mean key) of the listed pages: kernel launch.
+cudaError_t launch_centroids(kin_dtype dtype, int head_dim, int num_kv_heads,
+                             const void *k_pages, int64_t num_pages, const int32_t *page_ids,
+                             int64_t n, void *centroids, int32_t *err, cudaStream_t stream);
+
+struct ScoreParams {
+  const void *q;             // [B, H*G, d]
+  const void *centroids;     // [P, H, d]
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  float *scores;             // [B*H, max_blocks]
+  int32_t *sel;              // [B*H, top_k]
+  int32_t *err;
+  int64_t num_pages;
+  int batch, num_kv_heads, group, max_blocks, top_k;
+  int chunk;                 // candidate blocks scored per CTA
+};
+cudaError_t launch_score(kin_dtype dtype, int head_dim, const ScoreParams &p,
+                         cudaStream_t stream);
+cudaError_t launch_select(const ScoreParams &p, cudaStream_t stream);
+
+struct AttnParams {
+  const void *q;             // [B, H*G, d]
+  const void *k_pages;       // [P, H, 16, d] (SIMT path; the tensor-core path uses maps)
+  const void *v_pages;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *sel;        // [B*H, sel_stride] kept logical blocks, or NULL = every block
+  void *out;                 // [B, H*G, d]
+  float *lse;                // [B, H*G] or NULL
+  float *part_o;             // [B*H, max_splits, G, d] unnormalised partial outputs
+  float *part_ml;            // [B*H, max_splits, G, 2] (running max in log2 units, sum)
+  int32_t *counters;         // [B*H] split arrivals (zero between calls)
+  int32_t *err;
+  int64_t num_pages;
+  int batch, num_kv_heads, group, max_blocks, sel_stride;
+  int items_per_split;       // blocks handled by one CTA
+  int max_splits;
+  float sm_scale;
+};
+cudaError_t launch_attention(kin_dtype dtype, int head_dim, const AttnParams &p,
+                             const CUtensorMap *kmap, const CUtensorMap *vmap,
+                             cudaStream_t stream);
+
+// Tiling facts the host needs for workspace sizing and split planning.
+int attention_warps();
+int attention_max_items();
+
+}  // namespace kin

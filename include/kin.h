@@ -1,0 +1,175 @@
+/*
+ * kin.h -- block top-k (centroid-scored) sparse decode attention on B300 (sm_103a).
+ *
+ * The method: every 16-token key block of a paged KV cache is summarised by its mean
+ * key vector (its centroid); for one decode step, the blocks of each (sequence, KV head)
+ * row are scored by the dot product of that centroid with the query heads of the GQA
+ * group, summed over the group; the top-k blocks are kept and softmax attention runs
+ * over the kept blocks' keys and values only.  Sources:
+ *   - block top-k ranks key blocks by their mean key vectors and keeps the k best
+ *     blocks of each GQA query group -- Pith review of "Kinetics: Rethinking Test-Time
+ *     Scaling Laws", section "What carries the argument" (block top-k as the sparse
+ *     replacement of the quadratic KV term in the eFLOPs cost model C_TTS);
+ *   - block = KV page of 16 tokens, k counted in pages, one decoder layer of paged
+ *     decode, dense decode as the comparison -- Kinetics README, section "Benchmark
+ *     Block TopK Attention throughput" (--page_size 16 --topk_page 64).
+ * Readings where the pages are silent (identical in the library and in its tests):
+ *   - the group score is the SUM over the group's query heads of q_g . c_j;
+ *   - the final block (holding the current token, possibly partial) is always kept and
+ *     counts toward k; it is never scored; with nb <= k blocks every block is kept;
+ *   - equal scores go to the lower block index;
+ *   - sm_scale multiplies q.k inside the softmax; scoring is scale-free.
+ *
+ * Conventions for every entry point:
+ *   - All pointers inside the structs are DEVICE pointers (cudaMalloc'd or torch
+ *     tensors on the current device) unless stated otherwise; the structs themselves
+ *     live in host memory and are read during the call only.
+ *   - The library allocates no memory and never synchronises: all work is enqueued on
+ *     the given stream (a cudaStream_t; NULL = the legacy default stream) and runs
+ *     asynchronously.  The caller owns every buffer and keeps it alive until the
+ *     stream reaches the enqueued work.
+ *   - Arguments are validated on the host before anything is enqueued; a bad argument
+ *     returns a status and enqueues nothing.  kin_last_error() gives a one-line reason.
+ *   - Errors only the device can see (a block-table entry outside [0, num_pages), a
+ *     seq_len outside [1, 16 * max_blocks]) are OR-ed into *err_flag (KIN_DEVERR_*
+ *     bits) when err_flag is non-NULL; the offending block or row is skipped (a skipped
+ *     row gets zero output and lse = -inf).  Kernels never trap and never wait without
+ *     bound.
+ *   - Layout: K and V pages are [num_pages, num_kv_heads, 16, head_dim], contiguous,
+ *     row-major; query head q_h uses KV head h / G with G = num_q_heads / num_kv_heads
+ *     (query heads of one group are consecutive).
+ *   - Supported: head_dim in {64, 128}; G in 1..16; dtype f32 or bf16 (the same for Q,
+ *     K, V, centroids and O).  Anything else returns KIN_ERR_UNSUPPORTED.
+ */
+#ifndef KIN_H
+#define KIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KIN_API __attribute__((visibility("default")))
+#else
+#define KIN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *kin_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  KIN_OK = 0,
+  KIN_ERR_INVALID_ARG = 1, /* NULL where required, negative size, bad shape        */
+  KIN_ERR_UNSUPPORTED = 2, /* head_dim / group / dtype / size outside the set above */
+  KIN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than kin_workspace_size  */
+  KIN_ERR_CUDA = 4         /* a CUDA runtime or driver call failed at enqueue time  */
+} kin_status;
+
+typedef enum { KIN_F32 = 0, KIN_BF16 = 1 } kin_dtype;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define KIN_DEVERR_PAGE_ID 1 /* a block-table or page-list entry outside [0, num_pages) */
+#define KIN_DEVERR_SEQ_LEN 2 /* a seq_len outside [1, 16 * max_blocks]                 */
+#define KIN_DEVERR_TIMEOUT 4 /* a bounded wait for an asynchronous copy gave up         */
+
+/* A paged KV cache of one attention layer (caller-owned device memory). */
+typedef struct {
+  kin_dtype dtype;
+  int32_t num_kv_heads;   /* H, >= 1                                                  */
+  int32_t head_dim;       /* d, 64 or 128                                             */
+  int32_t page_size;      /* tokens per page == tokens per block; must be 16          */
+  int64_t num_pages;      /* P; num_pages * num_kv_heads * 16 must stay below 2^31    */
+  const void *k_pages;    /* [P, H, 16, d], 16-byte aligned                           */
+  const void *v_pages;    /* [P, H, 16, d], 16-byte aligned                           */
+} kin_kv_cache;
+
+/* One decode step over a batch of sequences. */
+typedef struct {
+  int32_t batch;          /* B >= 1                                                   */
+  int32_t num_q_heads;    /* H * G                                                    */
+  int32_t max_blocks;     /* columns of block_table, 1..16384                          */
+  int32_t top_k;          /* k >= 1 blocks kept per (sequence, KV head); ignored by dense */
+  float sm_scale;         /* softmax scale (> 0), e.g. 1/sqrt(d)                      */
+  const void *q;          /* [B, H*G, d]                                              */
+  const int32_t *block_table; /* [B, max_blocks] physical page of logical block j      */
+  const int32_t *seq_lens;    /* [B] tokens incl. the current one; nb = ceil(L/16)     */
+  const void *centroids;  /* [P, H, d] block centroids (kin_centroids_build); dense: unused */
+  void *out;              /* [B, H*G, d] attention output                              */
+  float *lse;             /* optional [B, H*G]: natural-log sum of exp(sm_scale * q.k)  */
+  int32_t *sel_blocks;    /* optional [B, H, top_k]: kept logical blocks, ascending,
+                             -1 padded when nb < k (block top-k only)                   */
+  float *scores;          /* optional [B, H, max_blocks]: group scores of blocks
+                             0..nb-2 of rows with nb > k (other entries untouched)      */
+  void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned,
+                             ZERO-FILLED before its first use (kin_workspace_init); the
+                             library leaves it zero-filled again after every call.  One
+                             workspace per stream: calls that overlap must not share it */
+  size_t workspace_bytes;
+  int32_t *err_flag;      /* optional device int; KIN_DEVERR_* bits are OR-ed in       */
+} kin_decode_args;
+
+/* Human-readable name of a status. Never NULL. */
+KIN_API const char *kin_status_str(kin_status s);
+
+/* One-line description of the last failed call on this host thread ("" if none). */
+KIN_API const char *kin_last_error(void);
+
+/* Bytes of workspace that kin_blocktopk_decode / kin_dense_decode need for these
+ * shapes (pointers inside the structs are not read).  The dense and the block top-k
+ * call may share one workspace sized for the larger of the two (mode 0 = block top-k,
+ * mode 1 = dense). */
+KIN_API kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *args,
+                              int32_t mode, size_t *bytes);
+
+/* Zero-fill a workspace (a cudaMemsetAsync on `stream`; allocates nothing). */
+KIN_API kin_status kin_workspace_init(void *workspace, size_t bytes, kin_stream_t stream);
+
+/* Centroid (mean key) of every listed page, for every KV head:
+ *   centroids[p, h, :] = (sum_{t<16} K[p, h, t, :]) / 16
+ * summed in fp32 in ascending t, stored in cache->dtype (bf16: round-to-nearest-even).
+ * Blocks are ranked by this mean key -- Pith review, "What carries the argument".
+ * page_ids: device int32[n] physical page ids (pages must hold 16 valid tokens), or
+ * NULL for all pages 0..num_pages-1 (then n must equal num_pages).  centroids: device
+ * [num_pages, H, d]; only the listed pages' rows are written.  Ids outside
+ * [0, num_pages) are skipped and flagged in *err_flag (optional). */
+KIN_API kin_status kin_centroids_build(const kin_kv_cache *cache, const int32_t *page_ids, int64_t n,
+                               void *centroids, int32_t *err_flag, kin_stream_t stream);
+
+/* Same arithmetic as kin_centroids_build for the pages a decode step just completed
+ * (a page whose 16th token was written).  n may be 0 (nothing is enqueued). */
+KIN_API kin_status kin_centroids_append(const kin_kv_cache *cache, const int32_t *page_ids, int32_t n,
+                                void *centroids, int32_t *err_flag, kin_stream_t stream);
+
+/* One block top-k decode step: for every sequence b and KV head h with
+ * nb = ceil(seq_lens[b] / 16) blocks:
+ *   score   s_j = sum_g q[b, hG+g, :] . centroids[block_table[b, j], h, :],  j < nb-1
+ *   select  S = {nb-1} + the k-1 largest s_j (ties to lower j); all blocks if nb <= k
+ *   attend  out[b, hG+g, :] = softmax over the valid tokens of S of sm_scale * q.k, applied to V
+ * Pith review, "What carries the argument"; Kinetics README, "Benchmark Block TopK
+ * Attention throughput".  Needs args->centroids built for every complete block that
+ * can be scored (all blocks but the final one of each sequence). */
+KIN_API kin_status kin_blocktopk_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                                kin_stream_t stream);
+
+/* Dense paged decode over every block (the comparison baseline): the attend step of
+ * kin_blocktopk_decode with S = all blocks.  args->top_k, centroids, sel_blocks and
+ * scores are ignored. */
+KIN_API kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                            kin_stream_t stream);
+
+/* Measurement variant of kin_blocktopk_decode (mode 0) or kin_dense_decode (mode 1):
+ * identical work, plus cudaEventRecord of the caller's events on `stream` around the
+ * kernels: events[0] before the first kernel, events[1] after scoring, events[2] after
+ * selection, events[3] after attention (dense: events[1] and [2] are recorded right
+ * after events[0]).  events: host array of 4 created cudaEvent_t handles.  Used to
+ * time each kernel of a step without a profiler. */
+KIN_API kin_status kin_decode_timed(const kin_kv_cache *cache, const kin_decode_args *args,
+                                    int32_t mode, void *const *events, kin_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KIN_H */

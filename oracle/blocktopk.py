@@ -5,10 +5,10 @@ may import this module.  It shares nothing with the CUDA path.
 
 What the method computes, and where the pages say so:
 
-* Block top-k attention "scores key blocks by their averaged key vectors and retrieves
-  only the top k blocks per query group" (Pith review of "Kinetics: Rethinking Test-Time
-  Scaling Laws", section "What carries the argument").  The averaged key of a block is
-  its centroid; the query group is the set of query heads sharing one KV head (GQA).
+* Block top-k attention ranks each key block by the mean of its key vectors and keeps
+  only the k best blocks for each query group (Pith review of "Kinetics: Rethinking
+  Test-Time Scaling Laws", section "What carries the argument").  The mean key of a block
+  is its centroid; the query group is the set of query heads sharing one KV head (GQA).
 * A block is one KV page of 16 tokens and k is counted in pages (Kinetics README,
   section "Benchmark Block TopK Attention throughput": ``--page_size 16 --topk_page 64``),
   and the benchmark is a paged decode of one decoder layer (same section).
@@ -71,12 +71,12 @@ def _store(x32: np.ndarray, store: str) -> np.ndarray:
 
 
 # --------------------------------------------------------------------------------------
-# Step 1: block centroid (averaged key vector)
+# Step 1: block centroid (mean key vector)
 # --------------------------------------------------------------------------------------
 def block_centroid(keys: np.ndarray, store: str = "f32") -> np.ndarray:
     """Mean of one block's 16 key vectors.
 
-    "scores key blocks by their averaged key vectors" (Pith review, "What carries the
+    Blocks are ranked by the mean of their keys (Pith review, "What carries the
     argument").  keys: [16, d] float32 values of one (page, KV head).  Summed in float32
     in ascending token order, multiplied by 1/16 (a power of two, so exact), rounded to
     the storage type.
@@ -112,8 +112,8 @@ def centroids(k_pages: np.ndarray, page_ids: Sequence[int], store: str) -> np.nd
 def group_scores(q_group: np.ndarray, cents: np.ndarray) -> np.ndarray:
     """s_j = sum over the group's query heads g of (q_g . c_j), in float64.
 
-    "retrieves only the top k blocks per query group" (Pith review, "What carries the
-    argument"): one score per block for the whole GQA group; the aggregation over the
+    Selection happens once per GQA query group (Pith review, "What carries the
+    argument"), so there is one score per block for the whole group; the aggregation over the
     group is a sum (reading 1).  q_group: [G, d]; cents: [n, d]; returns [n].
     """
     q = np.asarray(q_group, dtype=np.float64)
@@ -130,7 +130,7 @@ def group_scores(q_group: np.ndarray, cents: np.ndarray) -> np.ndarray:
 def select_blocks(scores: Sequence[float], nb: int, k: int) -> List[int]:
     """Logical block ids kept for one (sequence, KV head) row, ascending.
 
-    top-k blocks per query group (Pith review, "What carries the argument"); k counted in
+    the k best blocks per query group (Pith review, "What carries the argument"); k counted in
     pages (Kinetics README, "Benchmark Block TopK Attention throughput").  The final
     block nb-1 is always kept and counts toward k (reading 2); the other k-1 are the
     highest-scoring of blocks 0..nb-2, ties to the lower index (reading 3).  With

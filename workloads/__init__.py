@@ -56,7 +56,7 @@ class Config:
     head_dim: int
     top_k: int
     dtype: str                  # "f32" or "bf16": storage of Q, K, V, centroids and O
-    ctx_kind: str               # "uniform" | "ragged" | "best_of_n"
+    ctx_kind: str               # "uniform" | "ragged" | "best_of_n" | "explicit"
     ctx_lo: int                 # uniform: the context; ragged / best_of_n: lower bound
     ctx_hi: int = 0             # ragged / best_of_n: upper bound (inclusive)
     prefix: int = 0             # best_of_n: shared prompt tokens (a multiple of 16)
@@ -65,6 +65,7 @@ class Config:
     shuffled: bool = True       # page table is a random permutation of the page pool
     steps: int = 1              # decode steps (best_of_n: tokens appended per sample)
     seed: int = 1234
+    lens: tuple = ()            # "explicit": the context of every sequence
 
     @property
     def group(self) -> int:
@@ -151,6 +152,9 @@ def _draw_lengths(cfg: Config) -> torch.Tensor:
     if cfg.ctx_kind == "best_of_n":
         gen = torch.randint(cfg.ctx_lo, cfg.ctx_hi + 1, (cfg.batch,), generator=g)
         return gen + cfg.prefix
+    if cfg.ctx_kind == "explicit":
+        assert len(cfg.lens) == cfg.batch
+        return torch.tensor(cfg.lens, dtype=torch.int64)
     raise ValueError(cfg.ctx_kind)
 
 
