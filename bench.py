@@ -156,12 +156,15 @@ def cpu_baseline(inp, cfg, seconds: float, rows_cap: int = 100000) -> dict:
     done = 0
     with limit:
         t0 = time.perf_counter()
-        for b, h in rows:
-            rp = W.row_problem(inp, b, h)
-            O.blocktopk_decode(rp["q"], rp["k_pages"], rp["v_pages"], rp["block_table"],
-                               rp["seq_lens"], cfg.sm_scale, cfg.top_k,
-                               store="bf16" if cfg.dtype == "bf16" else "f32")
-            done += 1
+        while True:                      # cycle over the sampled rows until the budget ends
+            for b, h in rows:
+                rp = W.row_problem(inp, b, h)
+                O.blocktopk_decode(rp["q"], rp["k_pages"], rp["v_pages"], rp["block_table"],
+                                   rp["seq_lens"], cfg.sm_scale, cfg.top_k,
+                                   store="bf16" if cfg.dtype == "bf16" else "f32")
+                done += 1
+                if time.perf_counter() - t0 >= seconds:
+                    break
             if time.perf_counter() - t0 >= seconds:
                 break
         el = time.perf_counter() - t0
