@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 METRIC = "block-top-k decode: seq-steps/s, achieved HBM GB/s vs peak, speedup vs dense"
 UNIT = "seq-steps/s"
 L2_FLUSH_BYTES = 256 << 20       # > 126 MB of L2
-ATTN_SOURCE = os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", "attention.cu")
+ATTN_SOURCE = os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", "decode_fused.cu")
 
 
 def parse():
@@ -255,9 +255,8 @@ def main() -> int:
     stream = torch.cuda.current_stream(dev)
 
     def sparse_step(evs):
-        K.centroids_append(cache, just_dev, cents, err_flag=err)
         K.decode_timed(cache, q, table, seq, cfg.sm_scale, evs, centroids=cents,
-                       top_k=cfg.top_k, out=out, workspace=ws, err_flag=err)
+                       top_k=cfg.top_k, out=out, workspace=ws, err_flag=err, append_final=True)
 
     def dense_step(evs):
         K.decode_timed(cache, q, table, seq, cfg.sm_scale, evs, dense=True, out=out,
@@ -288,7 +287,7 @@ def main() -> int:
         return dict(step_ms=step_ms, attn_ms=attn_ms, score_ms=score_ms, sel_ms=sel_ms,
                     launches=launches_per_step * n_steps)
 
-    per_step = 3 + (1 if just else 0)     # append (when a page completed) + 3 decode kernels
+    per_step = 1 if cfg.dtype == "bf16" else 3   # fused kernel, or score + select + attention
     clocks = ClockSampler(dev.index)
     sp = timed(sparse_step, args.warmup, args.steps, per_step)
     clk = clocks.stop()
@@ -306,9 +305,10 @@ def main() -> int:
 
     byt = kv_bytes(cfg, lens)
     es = 2 if cfg.dtype == "bf16" else 4
-    append_bytes = len(just) * H * (16 * d + d) * es
+    append_bytes = len(just) * H * d * es      # centroid writes; the keys are already on chip
     step_bytes = byt["kv"] + byt["centroids"] + byt["qo"] + append_bytes
-    attn_bytes = byt["kv"] + byt["qo"]
+    # bf16: one fused kernel does the whole step; fp32: the attention kernel dominates
+    attn_bytes = step_bytes if cfg.dtype == "bf16" else byt["kv"] + byt["qo"]
     attn_s = statistics.mean(sp["attn_ms"]) / 1e3
     peak, peak_kind = peaks()
     achieved = attn_bytes / attn_s / 1e9
@@ -324,9 +324,8 @@ def main() -> int:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             q.copy_(q_host, non_blocking=True)
-            K.centroids_append(cache, just_dev, cents, err_flag=err)
             K.blocktopk_decode(cache, q, table, seq, cents, cfg.top_k, cfg.sm_scale, out=out,
-                               workspace=ws, err_flag=err)
+                               workspace=ws, err_flag=err, append_final=True)
             out_host.copy_(out, non_blocking=True)
             e1.record(stream)
             e1.synchronize()
@@ -353,9 +352,10 @@ def main() -> int:
                    "context": lens[0] if cfg.ctx_kind == "uniform" else "per-sequence",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "flushed (256 MB write) between timed steps, outside the timed events",
-                   "step": "centroid append of the pages the current token completed + block "
-                           "top-k decode (score, select, split-KV attention with fused merge)"},
-        "roofline": {"bound": "hbm", "kernel": "attn_bf16_kernel" if cfg.dtype == "bf16" else "attn_f32_kernel",
+                   "step": "one block top-k decode call: score, select, split-KV attention with "
+                           "merge, and the centroid append of the pages the current token "
+                           "completed (fused, one kernel for bf16)"},
+        "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel" if cfg.dtype == "bf16" else "attn_f32_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "bytes_per_launch": attn_bytes,

@@ -24,6 +24,8 @@ KIN_DEVERR_PAGE_ID = 1
 KIN_DEVERR_SEQ_LEN = 2
 KIN_DEVERR_TIMEOUT = 4
 
+KIN_DECODE_APPEND_FINAL = 1
+
 MODE_BLOCKTOPK = 0
 MODE_DENSE = 1
 
@@ -42,7 +44,7 @@ class DecodeArgs(ctypes.Structure):
                 ("block_table", c_void_p), ("seq_lens", c_void_p), ("centroids", c_void_p),
                 ("out", c_void_p), ("lse", c_void_p), ("sel_blocks", c_void_p),
                 ("scores", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-                ("err_flag", c_void_p)]
+                ("err_flag", c_void_p), ("flags", c_int32)]
 
 
 # Every function include/kin.h declares, with its ctypes signature.

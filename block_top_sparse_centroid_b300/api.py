@@ -182,7 +182,8 @@ def centroids_append(cache: PagedKVCache, page_ids: torch.Tensor, centroids: tor
 
 
 def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, top_k,
-            centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream, events=None):
+            centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream, events=None,
+            append_final=False):
     lib = L.load()
     dev = cache.device
     if q.dim() != 3:
@@ -200,8 +201,11 @@ def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, 
     _need(out, "out", (B, Hq, d), cache.dtype, dev)
     if lse is not None:
         _need(lse, "lse", (B, Hq), torch.float32, dev)
-    if mode == L.MODE_BLOCKTOPK:
+    if mode == L.MODE_BLOCKTOPK or append_final:
+        if centroids is None:
+            raise ValueError("centroids are required")
         _need(centroids, "centroids", (cache.num_pages, H, d), cache.dtype, dev)
+    if mode == L.MODE_BLOCKTOPK:
         if sel_blocks is not None:
             _need(sel_blocks, "sel_blocks", (B, H, top_k), torch.int32, dev)
         if scores is not None:
@@ -210,7 +214,9 @@ def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, 
     a.batch, a.num_q_heads, a.max_blocks, a.top_k = B, Hq, maxb, int(top_k)
     a.sm_scale = float(sm_scale)
     a.q, a.block_table, a.seq_lens = q.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr()
-    a.centroids = centroids.data_ptr() if (centroids is not None and mode == 0) else None
+    a.centroids = centroids.data_ptr() if (centroids is not None and
+                                           (mode == 0 or append_final)) else None
+    a.flags = L.KIN_DECODE_APPEND_FINAL if append_final else 0
     a.out = out.data_ptr()
     a.lse = None if lse is None else lse.data_ptr()
     a.sel_blocks = None if (sel_blocks is None or mode != 0) else sel_blocks.data_ptr()
@@ -247,28 +253,38 @@ def blocktopk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Te
                      sel_blocks: Optional[torch.Tensor] = None,
                      scores: Optional[torch.Tensor] = None,
                      workspace: Optional[Workspace] = None,
-                     err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """One block top-k decode step (score, select, sparse attention): kin_blocktopk_decode."""
+                     err_flag: Optional[torch.Tensor] = None, stream=None,
+                     append_final: bool = False) -> torch.Tensor:
+    """One block top-k decode step (score, select, sparse attention): kin_blocktopk_decode.
+
+    append_final: also write the centroid of each sequence's final block when that block
+    is complete (KIN_DECODE_APPEND_FINAL), i.e. the append the next steps need."""
     return _decode(L.MODE_BLOCKTOPK, cache, q, block_table, seq_lens, sm_scale, top_k,
-                   centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream)
+                   centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream,
+                   append_final=append_final)
 
 
 def decode_timed(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, sm_scale: float, events, dense: bool = False,
                  centroids: Optional[torch.Tensor] = None, top_k: int = 1,
                  out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
-                 err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                 err_flag: Optional[torch.Tensor] = None, stream=None,
+                 append_final: bool = False) -> torch.Tensor:
     """One decode step that also records 4 torch.cuda.Events around its kernels
     (before scoring, after scoring, after selection, after attention): kin_decode_timed."""
     mode = L.MODE_DENSE if dense else L.MODE_BLOCKTOPK
     return _decode(mode, cache, q, block_table, seq_lens, sm_scale, top_k, centroids, out,
-                   None, None, None, workspace, err_flag, stream, events=list(events))
+                   None, None, None, workspace, err_flag, stream, events=list(events),
+                   append_final=append_final)
 
 
 def dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
                  seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
                  lse: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
-                 err_flag: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                 err_flag: Optional[torch.Tensor] = None, stream=None,
+                 centroids: Optional[torch.Tensor] = None,
+                 append_final: bool = False) -> torch.Tensor:
     """Dense paged decode over every block (the comparison baseline): kin_dense_decode."""
-    return _decode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, None, out,
-                   lse, None, None, workspace, err_flag, stream)
+    return _decode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, centroids,
+                   out, lse, None, None, workspace, err_flag, stream,
+                   append_final=append_final)

@@ -35,11 +35,13 @@ kin_status cuda_fail(cudaError_t e, const char *what) {
 // attention CTAs over the 148 SMs of a B300 at three resident CTAs per SM.
 constexpr int kPlanSMs = 148;
 constexpr int kPlanCtasPerSM = 3;
-constexpr int kMaxItemsPerSplit = 256;
+constexpr int kMaxItemsPerSplit = 64;
 constexpr int kMaxBlocksLimit = 16384;
 
 struct Plan {
-  int rows, group, max_items, items_per_split, max_splits, score_chunk;
+  int rows, group, max_items, items_per_split, max_splits;
+  int score_chunk;      // fp32 standalone score kernel: candidates per CTA
+  int chunks_per_row;   // bf16 fused kernel: score items per row
 };
 
 Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
@@ -48,7 +50,9 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   pl.group = a->num_q_heads / c->num_kv_heads;
   pl.max_items = mode == 0 ? (a->top_k < a->max_blocks ? a->top_k : a->max_blocks) : a->max_blocks;
   const int warps = attention_warps();
-  const int target = kPlanSMs * kPlanCtasPerSM * 2;
+  // About four attention work items per resident CTA: enough for the work queue (bf16)
+  // or the wave tail (fp32) to balance, few enough that the per-item start-up is small.
+  const int target = kPlanSMs * kPlanCtasPerSM * 4;
   int splits = (target + pl.rows - 1) / pl.rows;
   const int max_useful = (pl.max_items + 2 * warps - 1) / (2 * warps);  // >= 2 blocks per warp
   if (splits > max_useful) splits = max_useful;
@@ -58,13 +62,14 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   if (ips > kMaxItemsPerSplit) ips = kMaxItemsPerSplit;
   pl.items_per_split = ips;
   pl.max_splits = (pl.max_items + ips - 1) / ips;
-  // Score chunk: about 8 CTAs per SM over all candidate blocks, 64..1024 per CTA.
+  // fp32 score kernel: about 8 CTAs per SM over all candidate blocks, 64..1024 per CTA.
   const long long cand = static_cast<long long>(pl.rows) * a->max_blocks;
   long long chunk = (cand + kPlanSMs * 8 - 1) / (kPlanSMs * 8);
   chunk = (chunk + 63) / 64 * 64;
   if (chunk < 64) chunk = 64;
   if (chunk > 1024) chunk = 1024;
   pl.score_chunk = static_cast<int>(chunk);
+  pl.chunks_per_row = mode == 0 ? (a->max_blocks - 1 + fused_chunk() - 1) / fused_chunk() : 0;
   return pl;
 }
 
@@ -77,8 +82,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &pl, int mode) {
   Layout L{};
   size_t off = 0;
-  L.counters = off;
-  off = align256(off + sizeof(int32_t) * pl.rows);
+  L.counters = off;   // score_cnt[rows], attn_cnt[rows], ready[rows], work_next, done_cnt
+  off = align256(off + sizeof(int32_t) * (3 * static_cast<size_t>(pl.rows) + 2));
   L.part_ml = off;
   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group);
   L.part_o = off;
@@ -135,7 +140,9 @@ kin_status check_args(const kin_kv_cache *c, const kin_decode_args *a, int mode)
   if (a->q == nullptr || a->block_table == nullptr || a->seq_lens == nullptr || a->out == nullptr)
     return fail(KIN_ERR_INVALID_ARG, "q / block_table / seq_lens / out must not be NULL");
   if (!aligned16(a->q)) return fail(KIN_ERR_INVALID_ARG, "q must be 16-byte aligned");
-  if (mode == 0) {
+  if ((a->flags & ~KIN_DECODE_APPEND_FINAL) != 0)
+    return fail(KIN_ERR_INVALID_ARG, "unknown flags 0x%x", static_cast<unsigned>(a->flags));
+  if (mode == 0 || (a->flags & KIN_DECODE_APPEND_FINAL) != 0) {
     if (a->centroids == nullptr) return fail(KIN_ERR_INVALID_ARG, "centroids must not be NULL");
     if (!aligned16(a->centroids)) return fail(KIN_ERR_INVALID_ARG, "centroids must be 16-byte aligned");
   }
@@ -231,17 +238,67 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   s = use_device_of(c->k_pages);
   if (s != KIN_OK) return s;
   uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+  int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.counters);
+  float *scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
+  int32_t *sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
+  const int append = (a->flags & KIN_DECODE_APPEND_FINAL) != 0;
   if ((s = record(events, 0, stream)) != KIN_OK) return s;
 
-  const int32_t *sel = nullptr;
+  if (c->dtype == KIN_BF16) {
+    CUtensorMap kmap, vmap;
+    s = encode_page_map(&kmap, c, c->k_pages);
+    if (s != KIN_OK) return s;
+    s = encode_page_map(&vmap, c, c->v_pages);
+    if (s != KIN_OK) return s;
+    FusedParams fp{};
+    fp.q = static_cast<const __nv_bfloat16 *>(a->q);
+    fp.centroids = static_cast<const __nv_bfloat16 *>(a->centroids);
+    fp.cent_out = static_cast<__nv_bfloat16 *>(a->centroids);
+    fp.block_table = a->block_table;
+    fp.seq_lens = a->seq_lens;
+    fp.out = a->out;
+    fp.lse = a->lse;
+    fp.scores = scores;
+    fp.sel = sel;
+    fp.part_o = reinterpret_cast<float *>(ws + L.part_o);
+    fp.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
+    fp.score_cnt = cnt;
+    fp.attn_cnt = cnt + pl.rows;
+    fp.ready = cnt + 2 * pl.rows;
+    fp.work_next = cnt + 3 * pl.rows;
+    fp.done_cnt = cnt + 3 * pl.rows + 1;
+    fp.err = a->err_flag;
+    fp.num_pages = c->num_pages;
+    fp.batch = a->batch;
+    fp.num_kv_heads = c->num_kv_heads;
+    fp.group = pl.group;
+    fp.max_blocks = a->max_blocks;
+    fp.top_k = mode == 0 ? a->top_k : 0;
+    fp.chunks_per_row = pl.chunks_per_row;
+    fp.items_per_split = pl.items_per_split;
+    fp.splits_per_row = pl.max_splits;
+    fp.n_score_items = mode == 0 ? pl.rows * pl.chunks_per_row : 0;
+    fp.n_attn_items = pl.rows * pl.max_splits;
+    fp.append_final = append;
+    fp.sm_scale = a->sm_scale;
+    if ((s = record(events, 1, stream)) != KIN_OK) return s;
+    if ((s = record(events, 2, stream)) != KIN_OK) return s;
+    cudaError_t e = launch_fused(c->head_dim, fp, &kmap, &vmap, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel launch");
+    if ((s = record(events, 3, stream)) != KIN_OK) return s;
+    return ok();
+  }
+
+  // fp32: standalone score, select and CUDA-core attention kernels.
+  const int32_t *kept = nullptr;
   if (mode == 0) {
     ScoreParams sp{};
     sp.q = a->q;
     sp.centroids = a->centroids;
     sp.block_table = a->block_table;
     sp.seq_lens = a->seq_lens;
-    sp.scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
-    sp.sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
+    sp.scores = scores;
+    sp.sel = sel;
     sp.err = a->err_flag;
     sp.num_pages = c->num_pages;
     sp.batch = a->batch;
@@ -256,24 +313,24 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     e = launch_select(sp, stream);
     if (e != cudaSuccess) return cuda_fail(e, "select kernel launch");
     if ((s = record(events, 2, stream)) != KIN_OK) return s;
-    sel = sp.sel;
+    kept = sel;
   } else {
     if ((s = record(events, 1, stream)) != KIN_OK) return s;
     if ((s = record(events, 2, stream)) != KIN_OK) return s;
   }
-
   AttnParams ap{};
   ap.q = a->q;
   ap.k_pages = c->k_pages;
   ap.v_pages = c->v_pages;
   ap.block_table = a->block_table;
   ap.seq_lens = a->seq_lens;
-  ap.sel = sel;
+  ap.sel = kept;
   ap.out = a->out;
   ap.lse = a->lse;
+  ap.cent_out = a->centroids;
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
   ap.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
-  ap.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  ap.counters = cnt + pl.rows;
   ap.err = a->err_flag;
   ap.num_pages = c->num_pages;
   ap.batch = a->batch;
@@ -283,17 +340,9 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   ap.sel_stride = mode == 0 ? a->top_k : 0;
   ap.items_per_split = pl.items_per_split;
   ap.max_splits = pl.max_splits;
+  ap.append_final = append;
   ap.sm_scale = a->sm_scale;
-  CUtensorMap kmap, vmap;
-  std::memset(&kmap, 0, sizeof(kmap));
-  std::memset(&vmap, 0, sizeof(vmap));
-  if (c->dtype == KIN_BF16) {
-    s = encode_page_map(&kmap, c, c->k_pages);
-    if (s != KIN_OK) return s;
-    s = encode_page_map(&vmap, c, c->v_pages);
-    if (s != KIN_OK) return s;
-  }
-  cudaError_t e = launch_attention(c->dtype, c->head_dim, ap, &kmap, &vmap, stream);
+  cudaError_t e = launch_attention_f32(c->head_dim, ap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
   if ((s = record(events, 3, stream)) != KIN_OK) return s;
   return ok();

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -33,13 +34,14 @@ cudaError_t launch_select(const ScoreParams &p, cudaStream_t stream);
 
 struct AttnParams {
   const void *q;             // [B, H*G, d]
-  const void *k_pages;       // [P, H, 16, d] (SIMT path; the tensor-core path uses maps)
+  const void *k_pages;       // [P, H, 16, d]
   const void *v_pages;
   const int32_t *block_table;
   const int32_t *seq_lens;
   const int32_t *sel;        // [B*H, sel_stride] kept logical blocks, or NULL = every block
   void *out;                 // [B, H*G, d]
   float *lse;                // [B, H*G] or NULL
+  void *cent_out;            // centroid table written when append_final is set
   float *part_o;             // [B*H, max_splits, G, d] unnormalised partial outputs
   float *part_ml;            // [B*H, max_splits, G, 2] (running max in log2 units, sum)
   int32_t *counters;         // [B*H] split arrivals (zero between calls)
@@ -48,14 +50,45 @@ struct AttnParams {
   int batch, num_kv_heads, group, max_blocks, sel_stride;
   int items_per_split;       // blocks handled by one CTA
   int max_splits;
+  int append_final;
   float sm_scale;
 };
-cudaError_t launch_attention(kin_dtype dtype, int head_dim, const AttnParams &p,
-                             const CUtensorMap *kmap, const CUtensorMap *vmap,
-                             cudaStream_t stream);
+// fp32 caches: CUDA-core split-KV attention (grid = max_splits x rows).
+cudaError_t launch_attention_f32(int head_dim, const AttnParams &p, cudaStream_t stream);
+
+// bf16 caches: one persistent kernel for score + select + attention (+ final-block append).
+struct FusedParams {
+  const __nv_bfloat16 *q;          // [B, H*G, d]
+  const __nv_bfloat16 *centroids;  // [P, H, d]
+  __nv_bfloat16 *cent_out;         // centroid table written when append_final is set
+  const int32_t *block_table;      // [B, max_blocks]
+  const int32_t *seq_lens;         // [B]
+  void *out;                       // [B, H*G, d]
+  float *lse;                      // [B, H*G] or NULL
+  float *scores;                   // [B*H, max_blocks]
+  int32_t *sel;                    // [B*H, top_k]
+  float *part_o;                   // [B*H, splits_per_row, G, d]
+  float *part_ml;                  // [B*H, splits_per_row, G, 2]
+  int32_t *score_cnt;              // [B*H] score-chunk arrivals
+  int32_t *attn_cnt;               // [B*H] split arrivals
+  int32_t *ready;                  // [B*H] selection published
+  int32_t *work_next;              // work-queue head
+  int32_t *done_cnt;               // finished CTAs
+  int32_t *err;
+  int64_t num_pages;
+  int batch, num_kv_heads, group, max_blocks;
+  int top_k;                       // 0 = dense decode (every block, no scoring)
+  int chunks_per_row;              // score items per row
+  int items_per_split, splits_per_row;
+  int n_score_items, n_attn_items;
+  int append_final;
+  float sm_scale;
+};
+cudaError_t launch_fused(int head_dim, const FusedParams &p, const CUtensorMap *kmap,
+                         const CUtensorMap *vmap, cudaStream_t stream);
+int fused_chunk();
 
 // Tiling facts the host needs for workspace sizing and split planning.
 int attention_warps();
-int attention_max_items();
 
 }  // namespace kin

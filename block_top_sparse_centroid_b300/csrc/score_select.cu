@@ -1,4 +1,5 @@
-// Group scoring of candidate blocks and top-k block selection.
+// Group scoring of candidate blocks and top-k block selection as standalone kernels,
+// used for fp32 caches (bf16 caches score and select inside the fused decode kernel).
 //
 // Block top-k ranks key blocks by their mean key vectors and keeps, for each GQA query
 // group, only the k best blocks (Pith review of "Kinetics: Rethinking Test-Time Scaling
@@ -196,9 +197,7 @@ cudaError_t launch_score_t(const ScoreParams &p, cudaStream_t stream) {
 
 cudaError_t launch_score(kin_dtype dtype, int head_dim, const ScoreParams &p,
                          cudaStream_t stream) {
-  if (dtype == KIN_BF16)
-    return head_dim == 128 ? launch_score_t<__nv_bfloat16, 128>(p, stream)
-                           : launch_score_t<__nv_bfloat16, 64>(p, stream);
+  if (dtype != KIN_F32) return cudaErrorInvalidValue;  // bf16 scores in the fused kernel
   return head_dim == 128 ? launch_score_t<float, 128>(p, stream)
                          : launch_score_t<float, 64>(p, stream);
 }

@@ -95,7 +95,9 @@ typedef struct {
   const void *q;          /* [B, H*G, d]                                              */
   const int32_t *block_table; /* [B, max_blocks] physical page of logical block j      */
   const int32_t *seq_lens;    /* [B] tokens incl. the current one; nb = ceil(L/16)     */
-  const void *centroids;  /* [P, H, d] block centroids (kin_centroids_build); dense: unused */
+  void *centroids;        /* [P, H, d] block centroids (kin_centroids_build): read by block
+                             top-k; rows of complete final blocks written when flags has
+                             KIN_DECODE_APPEND_FINAL; unused by dense otherwise          */
   void *out;              /* [B, H*G, d] attention output                              */
   float *lse;             /* optional [B, H*G]: natural-log sum of exp(sm_scale * q.k)  */
   int32_t *sel_blocks;    /* optional [B, H, top_k]: kept logical blocks, ascending,
@@ -108,7 +110,15 @@ typedef struct {
                              workspace per stream: calls that overlap must not share it */
   size_t workspace_bytes;
   int32_t *err_flag;      /* optional device int; KIN_DEVERR_* bits are OR-ed in       */
+  int32_t flags;          /* KIN_DECODE_* bits, 0 for none                             */
 } kin_decode_args;
+
+/* Decode flag: when a sequence's final block is complete (seq_len a multiple of 16: the
+ * current token completed its page), also write that page's centroid into
+ * args->centroids, with the arithmetic of kin_centroids_append.  This is the append a
+ * decode step needs for later steps (the final block itself is never scored), done from
+ * the keys the attention already stages on chip, so it costs no extra HBM read. */
+#define KIN_DECODE_APPEND_FINAL 1
 
 /* Human-readable name of a status. Never NULL. */
 KIN_API const char *kin_status_str(kin_status s);

@@ -40,7 +40,7 @@ def device():
 class DeviceState:
     """Device copies of a workload plus its centroid table built by the library."""
 
-    def __init__(self, inp: W.Inputs, dev=None, build=True):
+    def __init__(self, inp: W.Inputs, dev=None, build=True, append=True):
         dev = dev or device()
         self.inp = inp
         self.dev = dev
@@ -64,21 +64,23 @@ class DeviceState:
                 K.centroids_build(self.cache, self.cents,
                                   page_ids=torch.tensor(before, dtype=torch.int32, device=dev),
                                   err_flag=self.err)
-            if just:
+            self.just_pages = just
+            if just and append:
                 K.centroids_append(self.cache, torch.tensor(just, dtype=torch.int32, device=dev),
                                    self.cents, err_flag=self.err)
 
     def refresh_q(self):
         self.q = self.inp.q.to(self.dev)
 
-    def decode(self, dense=False):
+    def decode(self, dense=False, append_final=False):
         cfg = self.inp.cfg
         B, Hq, H = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads
         out = torch.full((B, Hq, cfg.head_dim), float("nan"), dtype=self.q.dtype, device=self.dev)
         lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=self.dev)
         if dense:
             K.dense_decode(self.cache, self.q, self.table, self.lens, cfg.sm_scale, out=out,
-                           lse=lse, err_flag=self.err)
+                           lse=lse, err_flag=self.err, centroids=self.cents,
+                           append_final=append_final)
             torch.cuda.synchronize()
             return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy())
         sel = torch.full((B, H, cfg.top_k), -7, dtype=torch.int32, device=self.dev)
@@ -86,7 +88,7 @@ class DeviceState:
                             device=self.dev)
         K.blocktopk_decode(self.cache, self.q, self.table, self.lens, self.cents, cfg.top_k,
                            cfg.sm_scale, out=out, lse=lse, sel_blocks=sel, scores=scores,
-                           err_flag=self.err)
+                           err_flag=self.err, append_final=append_final)
         torch.cuda.synchronize()
         return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy(),
                     sel=sel.cpu().numpy(), scores=scores.cpu().numpy())

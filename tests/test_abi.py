@@ -63,7 +63,7 @@ int main(void) {
   F(kin_kv_cache, num_pages) F(kin_kv_cache, k_pages) F(kin_kv_cache, v_pages)
   F(kin_decode_args, sm_scale) F(kin_decode_args, q) F(kin_decode_args, centroids)
   F(kin_decode_args, scores) F(kin_decode_args, workspace) F(kin_decode_args, workspace_bytes)
-  F(kin_decode_args, err_flag)
+  F(kin_decode_args, err_flag) F(kin_decode_args, flags)
   return 0;
 }
 """)
@@ -132,6 +132,7 @@ def test_status_names(lib):
     (dict(args_kw=dict(q=0x3004)), L.KIN_ERR_INVALID_ARG),
     (dict(args_kw=dict(centroids=None)), L.KIN_ERR_INVALID_ARG),
     (dict(args_kw=dict(seq_lens=None)), L.KIN_ERR_INVALID_ARG),
+    (dict(args_kw=dict(flags=2)), L.KIN_ERR_INVALID_ARG),
     (dict(), L.KIN_ERR_WORKSPACE),                                   # no workspace
     (dict(args_kw=dict(workspace=0x10000, workspace_bytes=16)), L.KIN_ERR_WORKSPACE),
     (dict(args_kw=dict(workspace=0x10010, workspace_bytes=1 << 30)), L.KIN_ERR_WORKSPACE),
@@ -146,6 +147,8 @@ def test_host_validation_rejects(lib, case, status):
 def test_dense_ignores_topk_and_centroids(lib):
     c, a = _cache(), _args(top_k=0, centroids=None)
     assert _decode(lib, c, a, dense=True) == L.KIN_ERR_WORKSPACE   # got past the arguments
+    a.flags = L.KIN_DECODE_APPEND_FINAL                               # appending needs them
+    assert _decode(lib, c, a, dense=True) == L.KIN_ERR_INVALID_ARG
 
 
 def test_workspace_size(lib):

@@ -143,7 +143,9 @@ def test_repeat_calls_identical_and_workspace_left_clean():
     assert np.array_equal(d1["out"], d2["out"])
     import block_top_sparse_centroid_b300.api as A
     ws = A._default_ws[(st.dev.type, st.dev.index)].buf
-    assert int(ws[:4 * cfg.batch * cfg.num_kv_heads].view(torch.int32).abs().sum()) == 0
+    rows = cfg.batch * cfg.num_kv_heads
+    # arrival counters, ready flags, queue head and finished-CTA count: all back to zero
+    assert int(ws[:4 * (3 * rows + 2)].view(torch.int32).abs().sum()) == 0
 
 
 def test_centroid_build_all_pages_and_append():
@@ -194,3 +196,22 @@ def test_dense_multi_split_long_rows():
     cfg = _cfg("long", H=1, G=8, k=16, lens=(16384, 9001, 16 * 700 + 5), seed=13)
     _run(cfg, dense=True)
     _run(cfg)
+
+
+@pytest.mark.parametrize("dtype,d", [("bf16", 128), ("bf16", 64), ("f32", 64)])
+@pytest.mark.parametrize("dense", [False, True])
+def test_decode_appends_completed_final_blocks(dtype, d, dense):
+    # sequences whose current token completed their final page (L % 16 == 0) and others
+    lens = (32, 48, 1600, 1601, 16 * 77, 16 * 3 + 5)
+    cfg = _cfg("app", dtype=dtype, d=d, H=2, G=4, k=8, lens=lens, seed=17 + d)
+    inp = W.generate(cfg)
+    st = DeviceState(inp, append=False)         # final pages' centroids not built yet
+    assert st.just_pages
+    zero = st.cents[torch.tensor(st.just_pages, device=st.dev).long()]
+    assert int(zero.float().abs().sum()) == 0
+    res = st.decode(dense=dense, append_final=True)
+    torch.cuda.synchronize()
+    check_centroids(inp, st.cents, st.just_pages)
+    check_centroids(inp, st.cents, inp.complete_pages().tolist())
+    compare_rows(inp, res, all_rows(cfg), dense=dense)
+    assert st.error_bits() == 0
