@@ -235,15 +235,21 @@ __device__ void attention_item(const FusedParams &p, const CUtensorMap *kmap,
   const int b = row / H, h = row % H;
   const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, G, H};
   const int L = __ldg(p.seq_lens + b);
+  int32_t *srow_w = p.sel + static_cast<int64_t>(row) * p.top_k;
   if (L < 1 || L > kBlock * p.max_blocks) {
     if (split == 0) {
       write_empty_row<__nv_bfloat16, D>(ec, b, h);
       if (tid == 0 && h == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
+      for (int i = tid; i < p.top_k; i += kThreads) srow_w[i] = -1;
     }
     return;
   }
   const int nb = (L + kBlock - 1) / kBlock;
   const bool every_block = p.top_k == 0 || nb <= p.top_k;
+  if (p.top_k > 0 && nb <= p.top_k && split == 0) {
+    // no selection ran for this row: its kept list is every block, -1 padded
+    for (int i = tid; i < p.top_k; i += kThreads) srow_w[i] = i < nb ? i : -1;
+  }
   const int n_items = p.top_k == 0 ? nb : min(nb, p.top_k);
   const int splits = (n_items + p.items_per_split - 1) / p.items_per_split;
   if (split >= splits) return;
