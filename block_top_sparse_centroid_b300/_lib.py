@@ -53,7 +53,6 @@ SIGNATURES = {
     "kin_last_error": (c_char_p, []),
     "kin_workspace_size": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_int32,
                                    POINTER(c_size_t)]),
-    "kin_workspace_init": (c_int, [c_void_p, c_size_t, c_void_p]),
     "kin_centroids_build": (c_int, [POINTER(KvCache), c_void_p, c_int64, c_void_p, c_void_p,
                                     c_void_p]),
     "kin_centroids_append": (c_int, [POINTER(KvCache), c_void_p, c_int32, c_void_p, c_void_p,

@@ -109,7 +109,7 @@ def workspace_size(cache: PagedKVCache, batch: int, num_q_heads: int, max_blocks
 
 
 class Workspace:
-    """A zero-filled device scratch buffer that grows on demand (one per stream)."""
+    """A device scratch buffer that grows on demand (one per stream of decode calls)."""
 
     def __init__(self, device):
         self.device = torch.device(device)

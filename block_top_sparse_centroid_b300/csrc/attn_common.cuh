@@ -49,7 +49,7 @@ struct EmitCtx {
   float *lse;          // [B, H*G] or NULL
   float *part_o;       // [rows, max_splits, G, D]
   float *part_ml;      // [rows, max_splits, G, 2]
-  int32_t *counters;   // [rows] split arrivals, zero between calls
+  int32_t *counters;   // [rows] split arrivals, cleared before the kernel starts
   int max_splits;
   int G, H;
 };
@@ -129,7 +129,6 @@ __device__ void combine_and_emit(const EmitCtx &e, int row, int b, int h, int sp
   __syncthreads();
   if (*s_flag) {
     __threadfence();
-    if (threadIdx.x == 0) e.counters[row] = 0;  // leave the workspace zeroed
     const float *po_row = e.part_o + slot * G * D;
     const float *pml_row = e.part_ml + slot * G * 2;
     for (int x = threadIdx.x; x < G * D; x += blockDim.x) {

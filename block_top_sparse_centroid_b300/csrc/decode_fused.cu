@@ -215,7 +215,6 @@ __device__ void score_item(const FusedParams &p, int item, uint8_t *smem, Shared
   __syncthreads();
   if (!sh.flag) return;
   __threadfence();
-  if (tid == 0) p.score_cnt[row] = 0;              // leave the workspace zeroed
   select_row(srow, n, p.top_k - 1, nb, reinterpret_cast<uint32_t *>(smem), sh.cnt,
              sh.scan_tmp, p.sel + static_cast<int64_t>(row) * p.top_k);
   fence_proxy_async_smem();                        // keys area is reused by TMA copies
@@ -409,21 +408,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       attention_item<D>(p, &kmap, &vmap, item - p.n_score_items, smem, sh, uses, policy);
     if (tid == 0) sh.next = next;
     __syncthreads();
-  }
-  // The last CTA to finish leaves the queue and the ready flags zeroed for the next call.
-  if (tid == 0) {
-    __threadfence();
-    sh.flag = atomicAdd(p.done_cnt, 1) == static_cast<int>(gridDim.x) - 1;
-  }
-  __syncthreads();
-  if (sh.flag) {
-    __threadfence();
-    const int rows = p.batch * p.num_kv_heads;
-    for (int r = tid; r < rows; r += kThreads) p.ready[r] = 0;
-    if (tid == 0) {
-      *p.work_next = 0;
-      *p.done_cnt = 0;
-    }
   }
 }
 

@@ -73,6 +73,11 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   return pl;
 }
 
+// Arrival counters, ready flags and the work-queue head: cleared by every decode call.
+size_t counter_bytes(const Plan &pl) {
+  return sizeof(int32_t) * (3 * static_cast<size_t>(pl.rows) + 1);
+}
+
 struct Layout {
   size_t counters, part_ml, part_o, scores, sel, total;
 };
@@ -82,8 +87,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &pl, int mode) {
   Layout L{};
   size_t off = 0;
-  L.counters = off;   // score_cnt[rows], attn_cnt[rows], ready[rows], work_next, done_cnt
-  off = align256(off + sizeof(int32_t) * (3 * static_cast<size_t>(pl.rows) + 2));
+  L.counters = off;   // score_cnt[rows], attn_cnt[rows], ready[rows], work_next
+  off = align256(off + counter_bytes(pl));
   L.part_ml = off;
   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group);
   L.part_o = off;
@@ -243,6 +248,9 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   int32_t *sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
   const int append = (a->flags & KIN_DECODE_APPEND_FINAL) != 0;
   if ((s = record(events, 0, stream)) != KIN_OK) return s;
+  // The workspace is scratch shared with calls of other shapes: clear the counters.
+  cudaError_t me = cudaMemsetAsync(cnt, 0, counter_bytes(pl), stream);
+  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync of the workspace counters");
 
   if (c->dtype == KIN_BF16) {
     CUtensorMap kmap, vmap;
@@ -266,7 +274,6 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.attn_cnt = cnt + pl.rows;
     fp.ready = cnt + 2 * pl.rows;
     fp.work_next = cnt + 3 * pl.rows;
-    fp.done_cnt = cnt + 3 * pl.rows + 1;
     fp.err = a->err_flag;
     fp.num_pages = c->num_pages;
     fp.batch = a->batch;
@@ -399,14 +406,6 @@ kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *
     return fail(KIN_ERR_INVALID_ARG, "bad shapes for workspace sizing");
   const Plan pl = make_plan(cache, args, mode);
   *bytes = make_layout(cache, args, pl, mode).total;
-  return ok();
-}
-
-kin_status kin_workspace_init(void *workspace, size_t bytes, kin_stream_t stream) {
-  using namespace kin;
-  if (workspace == nullptr) return fail(KIN_ERR_INVALID_ARG, "workspace is NULL");
-  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return ok();
 }
 

@@ -44,7 +44,7 @@ struct AttnParams {
   void *cent_out;            // centroid table written when append_final is set
   float *part_o;             // [B*H, max_splits, G, d] unnormalised partial outputs
   float *part_ml;            // [B*H, max_splits, G, 2] (running max in log2 units, sum)
-  int32_t *counters;         // [B*H] split arrivals (zero between calls)
+  int32_t *counters;         // [B*H] split arrivals (cleared before the kernel starts)
   int32_t *err;
   int64_t num_pages;
   int batch, num_kv_heads, group, max_blocks, sel_stride;
@@ -73,7 +73,6 @@ struct FusedParams {
   int32_t *attn_cnt;               // [B*H] split arrivals
   int32_t *ready;                  // [B*H] selection published
   int32_t *work_next;              // work-queue head
-  int32_t *done_cnt;               // finished CTAs
   int32_t *err;
   int64_t num_pages;
   int batch, num_kv_heads, group, max_blocks;

@@ -104,10 +104,10 @@ typedef struct {
                              -1 padded when nb < k (block top-k only)                   */
   float *scores;          /* optional [B, H, max_blocks]: group scores of blocks
                              0..nb-2 of rows with nb > k (other entries untouched)      */
-  void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned,
-                             ZERO-FILLED before its first use (kin_workspace_init); the
-                             library leaves it zero-filled again after every call.  One
-                             workspace per stream: calls that overlap must not share it */
+  void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned; its
+                             contents need no initialisation (each call first clears the
+                             few counters it uses, on `stream`).  Calls that may overlap
+                             on the GPU (other streams) must not share a workspace       */
   size_t workspace_bytes;
   int32_t *err_flag;      /* optional device int; KIN_DEVERR_* bits are OR-ed in       */
   int32_t flags;          /* KIN_DECODE_* bits, 0 for none                             */
@@ -132,9 +132,6 @@ KIN_API const char *kin_last_error(void);
  * mode 1 = dense). */
 KIN_API kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *args,
                               int32_t mode, size_t *bytes);
-
-/* Zero-fill a workspace (a cudaMemsetAsync on `stream`; allocates nothing). */
-KIN_API kin_status kin_workspace_init(void *workspace, size_t bytes, kin_stream_t stream);
 
 /* Centroid (mean key) of every listed page, for every KV head:
  *   centroids[p, h, :] = (sum_{t<16} K[p, h, t, :]) / 16

@@ -130,7 +130,7 @@ def test_page_permutation_invariance():
         assert np.array_equal(ra[key], rb[key]), key
 
 
-def test_repeat_calls_identical_and_workspace_left_clean():
+def test_repeat_calls_identical_and_dirty_workspace():
     cfg = _cfg("rep", H=8, G=2, k=8, lens=(4000,) * 8, seed=2)
     inp = W.generate(cfg)
     st = DeviceState(inp)
@@ -141,11 +141,12 @@ def test_repeat_calls_identical_and_workspace_left_clean():
     for key in ("out", "lse", "sel", "scores"):
         assert np.array_equal(r1[key], r2[key], equal_nan=True), key
     assert np.array_equal(d1["out"], d2["out"])
+    # a workspace left dirty by calls of other shapes gives the same answer
     import block_top_sparse_centroid_b300.api as A
-    ws = A._default_ws[(st.dev.type, st.dev.index)].buf
-    rows = cfg.batch * cfg.num_kv_heads
-    # arrival counters, ready flags, queue head and finished-CTA count: all back to zero
-    assert int(ws[:4 * (3 * rows + 2)].view(torch.int32).abs().sum()) == 0
+    A._default_ws[(st.dev.type, st.dev.index)].buf.fill_(0x5A)
+    r3 = st.decode()
+    for key in ("out", "lse", "sel", "scores"):
+        assert np.array_equal(r1[key], r3[key], equal_nan=True), key
 
 
 def test_centroid_build_all_pages_and_append():
