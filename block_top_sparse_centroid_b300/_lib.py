@@ -59,6 +59,7 @@ SIGNATURES = {
                                      c_void_p]),
     "kin_blocktopk_decode": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
     "kin_dense_decode": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
+    "kin_blocktopk_decode_static": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
     "kin_decode_timed": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_int32,
                                  POINTER(c_void_p), c_void_p]),
 }

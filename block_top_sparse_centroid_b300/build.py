@@ -15,7 +15,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkin.so")
 
-SOURCES = ["centroid.cu", "score_select.cu", "attention.cu", "decode_fused.cu", "kin_api.cu"]
+SOURCES = ["centroid.cu", "score_select.cu", "attention.cu", "decode_fused.cu", "kin_api.cu",
+           "noalloc.cu"]
 HEADERS = ["kin_common.cuh", "attn_common.cuh", "kin_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

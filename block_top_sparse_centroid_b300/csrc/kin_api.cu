@@ -375,6 +375,15 @@ kin_status run_centroids(const kin_kv_cache *c, const int32_t *page_ids, int64_t
 }
 
 }  // namespace
+
+kin_status set_error(kin_status s, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
 }  // namespace kin
 
 extern "C" {

@@ -90,4 +90,7 @@ int fused_chunk();
 // Tiling facts the host needs for workspace sizing and split planning.
 int attention_warps();
 
+// Record a one-line reason for kin_last_error() and return `s`.
+kin_status set_error(kin_status s, const char *fmt, ...);
+
 }  // namespace kin

@@ -166,6 +166,22 @@ KIN_API kin_status kin_blocktopk_decode(const kin_kv_cache *cache, const kin_dec
 KIN_API kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_args *args,
                             kin_stream_t stream);
 
+/* kin_blocktopk_decode for callers that cannot allocate device memory -- e.g. a server
+ * that gives all GPU memory to its KV-cache pool at start-up and allows no allocation
+ * afterwards, or a loop that must not let cudaMalloc/cudaFree synchronise the device.
+ * The paper has no counterpart: this is a property of the library, not of the method.
+ * Identical work and results; args->workspace / workspace_bytes are ignored and the
+ * scratch is instead a 16 MiB array inside the library, which every GPU that loads the
+ * library keeps until the process exits.  Shapes whose kin_workspace_size exceeds 16 MiB
+ * return KIN_ERR_WORKSPACE.  The first call on a device looks up the array's device
+ * address (with that device current); make that first call before any stream capture.
+ * All calls share the one array and it keeps the previous call's contents (each call
+ * clears the counters it needs first), so calls that may overlap on the GPU -- other
+ * streams, other host threads -- race and must not be issued. */
+KIN_API kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
+                                               const kin_decode_args *args,
+                                               kin_stream_t stream);
+
 /* Measurement variant of kin_blocktopk_decode (mode 0) or kin_dense_decode (mode 1):
  * identical work, plus cudaEventRecord of the caller's events on `stream` around the
  * kernels: events[0] before the first kernel, events[1] after scoring, events[2] after
