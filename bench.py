@@ -35,7 +35,7 @@ ATTN_SOURCE = os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", "deco
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1, help="workload index (0..4)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
@@ -263,27 +263,39 @@ def main() -> int:
                        workspace=wsd, err_flag=err)
 
     def timed(step_fn, n_warm, n_steps, launches_per_step):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n_steps)]
+        """Warm up eagerly, capture one step into a CUDA graph, then time n_steps replays.
+
+        The graph holds the step's counter memset and kernel(s) with external event-record
+        nodes around them, so every replay timestamps its own kernels on the device and
+        no host-side marshalling or launch latency falls inside the timed region."""
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
         for _ in range(n_warm):
             flush.zero_()
-            step_fn([torch.cuda.Event(enable_timing=True) for _ in range(4)])
+            step_fn(evs)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            step_fn(evs)
+        for _ in range(n_warm):
+            flush.zero_()
+            graph.replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
+        step_ms, attn_ms, score_ms, sel_ms = [], [], [], []
         for i in range(n_steps):
             flush.zero_()                       # L2 flush, outside the timed events
-            evs[i][4].record(stream)
-            step_fn(evs[i][:4])
-            evs[i][5].record(stream)
+            graph.replay()
+            evs[3].synchronize()
+            step_ms.append(evs[0].elapsed_time(evs[3]))
+            score_ms.append(evs[0].elapsed_time(evs[1]))
+            sel_ms.append(evs[1].elapsed_time(evs[2]))
+            attn_ms.append(evs[2].elapsed_time(evs[3]))
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize()
-        step_ms = [evs[i][4].elapsed_time(evs[i][5]) for i in range(n_steps)]
-        attn_ms = [evs[i][2].elapsed_time(evs[i][3]) for i in range(n_steps)]
-        score_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(n_steps)]
-        sel_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(n_steps)]
         return dict(step_ms=step_ms, attn_ms=attn_ms, score_ms=score_ms, sel_ms=sel_ms,
                     launches=launches_per_step * n_steps)
 

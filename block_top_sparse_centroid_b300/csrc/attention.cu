@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnParams p) 
   const int L = p.seq_lens[b];
   if (L < 1 || L > kBlock * p.max_blocks) {
     if (split == 0) {
-      write_empty_row<float, D>(ec, b, h);
+      write_empty_row<float, D, kThreads>(ec, b, h);
       if (tid == 0 && h == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
     }
     return;
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kThreads) attn_f32_kernel(const AttnParams p) 
     for (int i = 0; i < kPer; ++i) wo[(warp * kMaxGroup + g) * D + lane * kPer + i] = acc[g][i];
   }
   __syncthreads();
-  combine_and_emit<float, D>(ec, row, b, h, split, splits, wm, wl, wo, &s_flag);
+  combine_and_emit<float, D, kWarps, kMaxGroup, kThreads, CtaBarrier>(ec, row, b, h, split, splits, wm, wl, wo, &s_flag);
 }
 
 template <int D>

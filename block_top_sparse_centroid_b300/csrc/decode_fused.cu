@@ -1,48 +1,200 @@
-// One persistent kernel for a whole bf16 decode step: group scoring, top-k block
-// selection and split-KV attention, plus the centroid append of complete final blocks.
+// One persistent, warp-specialised kernel for a whole bf16 decode step: group scoring,
+// top-k block selection and split-KV attention, plus the centroid append of complete
+// final blocks.
 //
 // Block top-k ranks key blocks by their mean key vectors and keeps the k best blocks of
 // each GQA query group (Pith review of "Kinetics: Rethinking Test-Time Scaling Laws",
 // "What carries the argument"); blocks are 16-token pages and k counts pages (Kinetics
 // README, "Benchmark Block TopK Attention throughput").
 //
-// Work queue.  A global counter hands out items in this order:
-//   score items      (row, chunk of 256 candidate blocks), rows with nb > k only;
-//   attention items  (row, split of the row's kept-block list).
-// A score item writes s_j = (sum_g q_g) . c_j for its chunk; the last score item of a row
-// to finish (an atomic arrival count) selects the row's kept blocks and then releases
-// the row's ready flag.  An attention item of a row that needs selection waits on that
-// flag (bounded; a timeout sets KIN_DEVERR_TIMEOUT).  The wait cannot deadlock: every
-// score item is handed out before any attention item, and score items never wait, so
-// the item that completes a row is always held by a running CTA.
+// One CTA per SM: kProducers producer warps and 4 or 8 consumer warps around a ring of
+// shared-memory stages (160 KB).  HBM needs well over 100 KB in flight per SM to run near
+// its peak, and one thread issues a page's copies only every few hundred cycles, so four
+// producer warps run ahead of the consumers across work items, bounded only by the ring.
 //
-// Selection: radix select of the (k-1)-th largest order-preserving score key, 4 bits per
-// pass.  Each thread packs its digit counts into two 64-bit words (8 bits per digit),
-// each warp sums them with redux.sync, the CTA combines the 4 warps' 16 counts through
-// shared memory (one barrier per pass); then an index-ordered compaction emits the kept
-// blocks ascending, equal scores going to the lower block index.
-//
-// Attention: as in the standalone kernels -- TMA tiled copies of each kept page (K and V,
-// 64-column boxes, 128-byte swizzle) into per-warp shared-memory rings completed on
-// mbarriers, mma.m16n8k16 bf16 for S = Q K^T and O += P V with an online softmax, the
-// warps of a CTA combined in shared memory, and the row's splits merged by the last
-// split to arrive.
+// Work items, handed out by a global counter in this order:
+//   score items   (sequence, head range, chunk of candidate blocks).  The producer copies
+//                 each candidate's centroid rows for the head range (one contiguous
+//                 [heads, d] run per page) into the ring with bulk copies; the consumers
+//                 form s_j = (sum_g q_g) . c_j and store it.  The last consumer barrier of
+//                 the item publishes it with an arrival count per (sequence, head range).
+//   select items  (sequence, head range).  Each consumer warp takes rows of the range in
+//                 turn: it waits for the range's score items, runs a radix select over the
+//                 row's scores (8-bit digits, per-warp shared histograms), writes the kept
+//                 list ascending (equal scores to the lower block index, the final block
+//                 last) and releases the row's ready flag.
+//   attention     (row, split of the kept list).  The producer waits for the row's ready
+//                 flag, reads the split's kept blocks and their pages, and stages each
+//                 page's K and V (one TMA tiled copy each, 128-byte swizzle).  Producer
+//                 q stages pages q, q + kProducers, ... for its pipeline's consumer warps,
+//                 which compute S^T = K Q^T and O^T += V^T P^T with mma.m16n8k16 (bf16 in,
+//                 fp32 accumulate) and an online softmax; the warps' states are combined
+//                 in shared memory and the row's splits merged by the last split to
+//                 arrive (attn_common.cuh).
+// Every wait is bounded (a timeout sets KIN_DEVERR_TIMEOUT) and none can deadlock: a
+// CTA takes items in queue order, so every score item precedes every select item and
+// every select item precedes every attention item, in every CTA's own sequence of work;
+// score items wait for nothing but their own copies, select items only for score items,
+// attention items only for select items.
 #include "attn_common.cuh"
 #include "kin_internal.h"
 
 namespace kin {
 namespace {
 
-constexpr int kChunk = 256;          // candidate blocks per score item
-constexpr int kScoreUnroll = 8;      // centroid loads in flight per thread
-constexpr int kMaxKeys = 16384;      // selection keys (one per candidate) in shared memory
+constexpr int kProducers = 4;                       // producer warps = ring pipelines
+constexpr int kMaxRingBytes = 160 * 1024;
+constexpr int kMaxStages = kMaxRingBytes / (64 * 64);  // stages at d = 64
+constexpr int kDescs = 8;                           // descriptor slots producer -> consumers
+constexpr int kMaxScoreChunk = 256;                 // candidate blocks per score item
+constexpr int kHeadsPerRange = 32;                  // KV heads per score / select item
+// Consumer scratch: the combine buffers of an attention item, the group-summed queries
+// of a score item, or the histograms of the selections (never at once).
+constexpr int kScratchBytes = 34 * 1024;
+static_assert(kScratchBytes >= 8 * 8 * (128 + 2) * 4, "combine buffers, 8 warps x 8 heads");
+static_assert(kScratchBytes >= 4 * 16 * (128 + 2) * 4, "combine buffers, 4 warps x 16 heads");
+static_assert(kScratchBytes >= kHeadsPerRange * 128 * 4, "group-summed queries");
 
-// Dynamic shared memory: the attention stages, which also hold the selection keys and
-// the combine buffers (never at the same time).
-template <int D>
+// Launch shape for a head dimension D and NT n-tiles of 8 query heads (NT = 1: groups
+// of up to 8 query heads, NT = 2: up to 16).  kCW consumer warps (threads 0 .. 32 kCW - 1)
+// and kProducers producer warps after them; consumer warp w takes its pages from
+// pipeline w % kProducers, alternating with the other consumers of that pipeline.
+template <int D, int NT>
+struct Cfg {
+  static constexpr int kCW = NT == 1 ? 8 : 4;
+  static constexpr int kCThreads = kCW * 32;
+  static constexpr int kAllThreads = (kCW + kProducers) * 32;
+  static constexpr int kPPC = kCW / kProducers;    // consumers per pipeline
+  static constexpr int kQMax = 8 * NT;
+  using Bar = GroupBarrier<kCThreads>;
+  static_assert(kCW * kQMax * (D + 2) * 4 <= kScratchBytes, "combine buffers");
+  static_assert(kCW * 256 * 4 <= kScratchBytes, "selection histograms");
+};
+
+// The ring is split into one sub-ring per consumer warp.  Producer q stages the pages
+// (or score stages) q, q + kProducers, ... of every item, handing them in turn to its
+// consumer warps q, q + kProducers, ... (kPPC of them); each goes through that consumer's
+// sub-ring.  So every sub-ring has a single producer and a single consumer, both walk it
+// in the same order, and neither can get two laps ahead of the other (which the parity
+// waits of an mbarrier could not tell apart).
+template <int D, int NT>
+struct Ring {
+  static constexpr int kStageBytes = BfTile<D>::kStageBytes;   // K + V page of one head
+  static constexpr int kBytes = NT == 1 ? 128 * 1024 : kMaxRingBytes;
+  static constexpr int kStages = kBytes / kStageBytes;         // 16 / 32 or 20 / 40
+  static constexpr int kPer = kStages / Cfg<D, NT>::kCW;       // stages per consumer
+  static_assert(kStages <= kMaxStages && kStages % Cfg<D, NT>::kCW == 0, "stage arrays");
+  // shared-memory stage of consumer w's n-th page (or score stage), and its phase
+  __device__ static __forceinline__ int slot(int w, uint32_t n) { return w * kPer + n % kPer; }
+  __device__ static __forceinline__ uint32_t phase(uint32_t n) { return (n / kPer) & 1u; }
+};
+
+template <int D, int NT>
 constexpr size_t fused_smem_bytes() {
-  return BfTile<D>::kSmemBytes > kMaxKeys * 4 ? BfTile<D>::kSmemBytes : kMaxKeys * 4;
+  return 1024 + Ring<D, NT>::kBytes + kScratchBytes;   // 1024: alignment of the ring base
 }
+
+enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4 };
+enum : int { kAttnEveryBlock = 1, kAttnAppendLast = 2 };
+
+// A work item as the producer hands it to the consumers.
+struct Desc {
+  int kind;
+  int first;   // unused (kept 0)
+  int count;   // stages of the item (attention: pages)
+  int row;     // score / select: sequence b; attention / empty row: b * H + h
+  int x0;      // score / select: first head h0; attention: split
+  int x1;      // score: first candidate j0; select: candidates n; attention: splits
+  int x2;      // score / select: heads in the range; attention: kAttn* flags
+  int x3;      // tokens L of the sequence
+};
+
+struct FusedShared {
+  uint64_t full[kMaxStages];    // stage filled (producer arrival + copy bytes)
+  uint64_t empty[kMaxStages];   // stage consumed (one consumer warp)
+  uint64_t dfull[kDescs];       // descriptor written
+  uint64_t dempty[kDescs];      // descriptor read by every consumer warp
+  int4 meta[kMaxStages];        // attention: {page, ntok}; score: {j of first page, pages, valid mask}
+  Desc desc[kDescs];
+  int plist[kProducers][kMaxScoreChunk];  // producers: pages of the current score item
+  int flag;                     // consumers: last-arriver flag of the split merge
+  int abort;                    // set after a wait of this CTA timed out
+};
+
+// Bounded mbarrier wait.  After any wait of the CTA has timed out (a broken protocol),
+// later waits give up within a few hundred polls, so the CTA winds down quickly instead
+// of timing out wait by wait.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, FusedShared &sh,
+                                         int32_t *err) {
+  const uint32_t addr = smem_u32(bar);
+  for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0) return false;
+  }
+  *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+  flag_error(err, KIN_DEVERR_TIMEOUT);
+  return false;
+}
+
+// Bounded wait until *flag >= target (acquire).  Same abort rule as wait_bar.
+__device__ __forceinline__ bool wait_flag(const int32_t *flag, int target, FusedShared &sh,
+                                          int32_t *err) {
+  for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    if ((i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0) return false;
+    __nanosleep(64);
+  }
+  *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+  flag_error(err, KIN_DEVERR_TIMEOUT);
+  return false;
+}
+
+// Optional cycle counters per (CTA, warp) for tuning (compile with -DKIN_TRACE_CYCLES;
+// off in the library build).  Lane 0 of each warp accumulates clock64() deltas into slots.
+#ifdef KIN_TRACE_CYCLES
+constexpr int kTraceCtas = 160, kTraceWarps = 12, kTraceSlots = 16;
+__device__ unsigned long long g_trace[kTraceCtas * kTraceWarps * kTraceSlots];
+// Per-thread accumulators (registers / local memory), flushed once per warp at exit.
+struct TraceAcc {
+  long long v[kTraceSlots];
+};
+__device__ __forceinline__ void trace_flush(const TraceAcc &t) {
+  if ((threadIdx.x & 31) == 0 && blockIdx.x < kTraceCtas)
+    for (int i = 0; i < kTraceSlots; ++i)
+      g_trace[(blockIdx.x * kTraceWarps + (threadIdx.x >> 5)) * kTraceSlots + i] += t.v[i];
+}
+#define KIN_TRACE_DECL TraceAcc tr_ = {};
+#define KIN_TRACE_PARAM , TraceAcc &tr_
+#define KIN_TRACE_ARG , tr_
+#define KIN_TRACE_FLUSH trace_flush(tr_)
+#define KIN_TIC(name) const long long name = clock64()
+#define KIN_TOC(slot, name) (tr_.v[slot] += clock64() - (name))
+#define KIN_COUNT(slot, n) (tr_.v[slot] += (n))
+#else
+#define KIN_TRACE_DECL
+#define KIN_TRACE_PARAM
+#define KIN_TRACE_ARG
+#define KIN_TRACE_FLUSH
+#define KIN_TIC(v)
+#define KIN_TOC(slot, v)
+#define KIN_COUNT(slot, n)
+#endif
+// producer slots
+enum { kTrTotal = 0, kTrPWaitEmpty = 1, kTrPIssue = 2, kTrPMeta = 3, kTrPReady = 4, kTrPPush = 5,
+       kTrPPages = 6, kTrPItems = 7, kTrPNext = 8 };
+// consumer slots
+enum { kTrCWaitFull = 1, kTrCPage = 2, kTrCDesc = 3, kTrCEpilogue = 4, kTrCScore = 5,
+       kTrCSelect = 6, kTrCPages = 7, kTrCItems = 8, kTrCQ = 9, kTrCScoreQ = 10,
+       kTrCScoreWait = 11, kTrCEpiBar = 12, kTrCSelWait = 13, kTrCScoreComp = 14,
+       kTrCSelComp = 15 };
 
 __device__ __forceinline__ uint32_t score_key(float s) {
   if (s != s) return 0u;             // NaN ranks below every number
@@ -51,284 +203,588 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ int ld_acquire(const int32_t *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Kept blocks of one row: {nb-1} plus the m = k-1 largest of the n = nb-1 scores (ties to
-// the lower index), ascending, into out[0..k-1].  CTA-wide; keys: n words of shared memory.
-__device__ void select_row(const float *srow, int n, int m, int nb, uint32_t *keys,
-                           int (*s_cnt)[kWarps * 16], int *scan_tmp, int32_t *out) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int j = tid; j < n; j += kThreads) keys[j] = score_key(__ldcg(srow + j));
-  __syncthreads();
-  uint32_t prefix = 0u, mask = 0u;
-  int remaining = m;
+// Kept blocks of one row, by one warp: {nb-1} plus the m largest of the n scores
+// srow[0..n) (equal scores to the lower index), ascending, into out[0..m].  keys: room for
+// n words of shared memory, or NULL (every pass then re-reads srow); hist: 256 words.
+__device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *keys, int *hist,
+                            int32_t *out, int lane) {
+  if (keys != nullptr) {
+    for (int j = lane; j < n; j += 32) keys[j] = score_key(__ldcg(srow + j));
+    __syncwarp();
+  }
+  auto key_at = [&](int j) -> uint32_t {
+    return keys != nullptr ? keys[j] : score_key(__ldcg(srow + j));
+  };
+  if (m > 0) {
+    uint32_t prefix = 0u, mask = 0u;
+    int remaining = m;               // keys still to take at or below the current prefix
 #pragma unroll 1
-  for (int pass = 0; pass < 8; ++pass) {
-    const int shift = 28 - 4 * pass;
-    unsigned long long lo = 0ull, hi = 0ull;   // 8-bit count per digit (<= 128 keys/thread)
-    for (int j = tid; j < n; j += kThreads) {
-      const uint32_t key = keys[j];
-      if ((key & mask) == prefix) {
-        const uint32_t dg = (key >> shift) & 15u;
-        if (dg < 8) lo += 1ull << (8 * dg);
-        else hi += 1ull << (8 * (dg - 8));
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = lane; i < 256; i += 32) hist[i] = 0;
+      __syncwarp();
+      for (int j = lane; j < n; j += 32) {
+        const uint32_t key = key_at(j);
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
       }
-    }
-    int mine = 0;
+      __syncwarp();
+      int c[8], tot = 0;
 #pragma unroll
-    for (int d = 0; d < 16; ++d) {
-      const unsigned c = d < 8 ? static_cast<unsigned>((lo >> (8 * d)) & 255ull)
-                               : static_cast<unsigned>((hi >> (8 * (d - 8))) & 255ull);
-      const unsigned s = __reduce_add_sync(0xffffffffu, c);
-      if (lane == d) mine = static_cast<int>(s);
-    }
-    if (lane < 16) s_cnt[pass & 1][warp * 16 + lane] = mine;
-    __syncthreads();
-    int above = 0, digit = 0;
-    for (int d = 15; d >= 0; --d) {
-      int c = 0;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) c += s_cnt[pass & 1][w * 16 + d];
-      if (above + c >= remaining) {
-        digit = d;
-        break;
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[lane * 8 + i];
+        tot += c[i];
       }
-      above += c;
-    }
-    remaining -= above;
-    prefix |= static_cast<uint32_t>(digit) << shift;
-    mask |= 15u << shift;
-  }
-  const uint32_t thr = prefix;     // key of the m-th largest score
-  const int take_eq = remaining;   // keys equal to thr that are kept (>= 1)
-  const int per = (n + kThreads - 1) / kThreads;
-  const int lo_j = min(n, tid * per), hi_j = min(n, lo_j + per);
-  int gt = 0, eq = 0;
-  for (int j = lo_j; j < hi_j; ++j) {
-    const uint32_t key = keys[j];
-    gt += key > thr;
-    eq += key == thr;
-  }
-  int tot;
-  const int eq_before = block_exclusive_scan(eq, scan_tmp, &tot);
-  const int my_eq = max(0, min(eq, take_eq - eq_before));
-  int w = block_exclusive_scan(gt + my_eq, scan_tmp, &tot);
-  int used = 0;
-  for (int j = lo_j; j < hi_j; ++j) {
-    const uint32_t key = keys[j];
-    bool keep = key > thr;
-    if (key == thr && used < my_eq) {
-      keep = true;
-      ++used;
-    }
-    if (keep) out[w++] = j;
-  }
-  if (tid == 0) out[m] = nb - 1;
-}
-
-struct Shared {
-  uint64_t bars[kWarps * kStages];
-  int page[kMaxItems];
-  int ntok[kMaxItems];
-  int chunk_pages[kChunk];
-  int cnt[2][kWarps * 16];
-  int scan_tmp[32];
-  int next;
-  int flag;
-};
-
-template <int D>
-__device__ void score_item(const FusedParams &p, int item, uint8_t *smem, Shared &sh) {
-  constexpr int kVec = 8;                          // bf16 per 16-byte slice
-  constexpr int kTpi = D / kVec;                   // lanes per centroid (8 or 16)
-  constexpr int kGroups = kThreads / kTpi;         // centroids per CTA per load slot
-  const int tid = threadIdx.x;
-  const int row = item / p.chunks_per_row, chunk = item % p.chunks_per_row;
-  const int H = p.num_kv_heads, G = p.group;
-  const int b = row / H, h = row % H;
-  const int L = __ldg(p.seq_lens + b);
-  if (L < 1 || L > kBlock * p.max_blocks) {
-    if (chunk == 0 && h == 0 && tid == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
-    return;
-  }
-  const int nb = (L + kBlock - 1) / kBlock;
-  if (nb <= p.top_k) return;                       // every block kept: nothing to score
-  const int n = nb - 1;
-  const int j0 = chunk * kChunk;
-  if (j0 >= n) return;
-  const int j1 = min(n, j0 + kChunk);
-  const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-  for (int i = tid; i < j1 - j0; i += kThreads) sh.chunk_pages[i] = __ldg(trow + j0 + i);
-
-  const int grp = tid / kTpi, slice = tid % kTpi;
-  float qs[kVec], f[kVec];
-  const __nv_bfloat16 *qrow = p.q + (static_cast<int64_t>(b) * H * G + h * G) * D + slice * kVec;
-  Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qrow)), qs);
-  for (int g = 1; g < G; ++g) {
-    Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qrow + g * D)), f);
+      int incl = tot;                // keys in this lane's digits and all higher ones
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) qs[i] += f[i];
-  }
-  __syncthreads();
-  float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
-  for (int base = j0; base < j1; base += kGroups * kScoreUnroll) {
-    uint4 v[kScoreUnroll];
-    int jj[kScoreUnroll];
-    bool valid[kScoreUnroll];
-#pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      jj[u] = base + u * kGroups + grp;
-      valid[u] = false;
-      v[u] = make_uint4(0, 0, 0, 0);
-      if (jj[u] < j1) {
-        const int64_t page = sh.chunk_pages[jj[u] - j0];
-        if (page >= 0 && page < p.num_pages) {
-          valid[u] = true;
-          v[u] = ldg_stream(p.centroids + (page * H + h) * D + slice * kVec);
-        } else if (slice == 0) {
-          flag_error(p.err, KIN_DEVERR_PAGE_ID);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      const int above_lane = incl - tot;
+      const bool mine = above_lane < remaining && remaining <= incl;
+      int digit = 0, above = 0;
+      if (mine) {
+        int run = above_lane;
+        for (int i = 7; i >= 0; --i) {
+          if (run + c[i] >= remaining) {
+            digit = lane * 8 + i;
+            above = run;
+            break;
+          }
+          run += c[i];
         }
       }
+      const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      remaining -= above;
+      prefix |= static_cast<uint32_t>(digit) << shift;
+      mask |= 255u << shift;
+      __syncwarp();
     }
-#pragma unroll
-    for (int u = 0; u < kScoreUnroll; ++u) {
-      Elem<__nv_bfloat16>::unpack(v[u], f);
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < kVec; ++i) s = fmaf(qs[i], f[i], s);
-#pragma unroll
-      for (int o = kTpi / 2; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (slice == 0 && jj[u] < j1) __stcg(srow + jj[u], valid[u] ? s : -INFINITY);
+    const uint32_t thr = prefix;     // key of the m-th largest score
+    const int take_eq = remaining;   // keys equal to thr that are kept (>= 1)
+    const unsigned lt = (1u << lane) - 1u;
+    int written = 0, eq_seen = 0;
+    for (int base = 0; base < n; base += 32) {
+      const int j = base + lane;
+      const uint32_t key = j < n ? key_at(j) : 0u;
+      const bool gt = j < n && key > thr;
+      const bool eq = j < n && key == thr;
+      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+      const bool keep = gt || (eq && eq_seen + __popc(eqm & lt) < take_eq);
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      const int pos = written + __popc(km & lt);
+      if (keep && pos < m) out[pos] = j;
+      written += __popc(km);
+      eq_seen += __popc(eqm);
     }
   }
-  // Arrival; the last chunk of the row to finish selects.
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(p.score_cnt + row, 1);
-    sh.flag = (prev == (n + kChunk - 1) / kChunk - 1);
-  }
-  __syncthreads();
-  if (!sh.flag) return;
-  __threadfence();
-  select_row(srow, n, p.top_k - 1, nb, reinterpret_cast<uint32_t *>(smem), sh.cnt,
-             sh.scan_tmp, p.sel + static_cast<int64_t>(row) * p.top_k);
-  fence_proxy_async_smem();                        // keys area is reused by TMA copies
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) atomicExch(p.ready + row, 1);
+  if (lane == 0) out[m] = nb - 1;
 }
 
-template <int D>
-__device__ void attention_item(const FusedParams &p, const CUtensorMap *kmap,
-                               const CUtensorMap *vmap, int a, uint8_t *smem, Shared &sh,
-                               uint32_t &uses, uint64_t policy) {
-  using Tile = BfTile<D>;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = p.num_kv_heads, G = p.group;
-  const int row = a / p.splits_per_row, split = a % p.splits_per_row;
-  const int b = row / H, h = row % H;
-  const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, G, H};
-  const int L = __ldg(p.seq_lens + b);
-  int32_t *srow_w = p.sel + static_cast<int64_t>(row) * p.top_k;
-  if (L < 1 || L > kBlock * p.max_blocks) {
-    if (split == 0) {
-      write_empty_row<__nv_bfloat16, D>(ec, b, h);
-      if (tid == 0 && h == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
-      for (int i = tid; i < p.top_k; i += kThreads) srow_w[i] = -1;
+// The same selection with the row's keys held in registers: lane l holds the keys of
+// candidates j = l + 32 i, i < KPL (n <= 32 * KPL).  Every loop is unrolled, so the
+// passes run without shared-memory reloads of the keys.
+template <int KPL>
+__device__ void warp_select_reg(const float *srow, int n, int m, int nb, int *hist, int32_t *out,
+                                int lane) {
+  uint32_t key[KPL];
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const int j = lane + 32 * i;
+    key[i] = j < n ? score_key(__ldcg(srow + j)) : 0u;
+  }
+  if (m > 0) {
+    uint32_t prefix = 0u, mask = 0u;
+    int remaining = m;
+#pragma unroll 1
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      for (int i = lane; i < 256; i += 32) hist[i] = 0;
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) {
+        if (lane + 32 * i < n && (key[i] & mask) == prefix)
+          atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
+      }
+      __syncwarp();
+      int c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = hist[lane * 8 + i];
+        tot += c[i];
+      }
+      int incl = tot;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_down_sync(0xffffffffu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      const int above_lane = incl - tot;
+      const bool mine = above_lane < remaining && remaining <= incl;
+      int digit = 0, above = 0;
+      if (mine) {
+        int run = above_lane;
+        for (int i = 7; i >= 0; --i) {
+          if (run + c[i] >= remaining) {
+            digit = lane * 8 + i;
+            above = run;
+            break;
+          }
+          run += c[i];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+      digit = __shfl_sync(0xffffffffu, digit, src);
+      above = __shfl_sync(0xffffffffu, above, src);
+      remaining -= above;
+      prefix |= static_cast<uint32_t>(digit) << shift;
+      mask |= 255u << shift;
+      __syncwarp();
     }
-    return;
+    const uint32_t thr = prefix;
+    const int take_eq = remaining;
+    const unsigned lt = (1u << lane) - 1u;
+    int written = 0, eq_seen = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const bool in = lane + 32 * i < n;
+      const bool gt = in && key[i] > thr;
+      const bool eq = in && key[i] == thr;
+      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+      const bool keep = gt || (eq && eq_seen + __popc(eqm & lt) < take_eq);
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      const int pos = written + __popc(km & lt);
+      if (keep && pos < m) out[pos] = lane + 32 * i;
+      written += __popc(km);
+      eq_seen += __popc(eqm);
+    }
+  }
+  if (lane == 0) out[m] = nb - 1;
+}
+
+// ----------------------------------------------------------------------------------
+// Producer warps.  One thread issues one page's copies every few hundred cycles (barrier
+// wait, byte-count arrival, TMA issue), so kProducers warps share the work: producer q
+// stages the pages (attention) or ring stages (scores) i = q, q + kProducers, ... of every
+// item, which consumer warp q then processes.  Producer 0 also runs the work queue: it
+// turns items into descriptors.  In each warp lane 0 does the barrier and copy work and
+// the other lanes help read block tables and kept lists.
+// ----------------------------------------------------------------------------------
+
+// The descriptor of work item `item`; false when the item has nothing to do (an empty chunk or split, a row kept whole).
+template <int D>
+__device__ bool make_desc(const FusedParams &p, int item, Desc &d) {
+  const int H = p.num_kv_heads, HS = p.heads_per_range;
+  if (item < p.n_score_items) {
+    const int per_seq = p.head_ranges * p.chunks_per_seq;
+    const int b = item / per_seq, r = item % per_seq;
+    const int hr = r / p.chunks_per_seq, chunk = r % p.chunks_per_seq;
+    const int L = __ldg(p.seq_lens + b);
+    if (L < 1 || L > kBlock * p.max_blocks) return false;     // flagged by attention
+    const int nb = (L + kBlock - 1) / kBlock;
+    if (nb <= p.top_k) return false;                            // every block kept
+    const int j0 = chunk * p.score_chunk;
+    if (j0 >= nb - 1) return false;
+    const int npg = min(nb - 1, j0 + p.score_chunk) - j0;
+    const int h0 = hr * HS, hs = min(HS, H - h0);
+    const int pps = BfTile<D>::kStageBytes / (hs * D * 2);    // pages per stage
+    d = Desc{kDescScore, 0, (npg + pps - 1) / pps, b, h0, j0, hs, L};
+    return true;
+  }
+  if (item < p.n_score_items + p.n_select_items) {
+    const int it = item - p.n_score_items;
+    const int b = it / p.head_ranges, hr = it % p.head_ranges;
+    const int L = __ldg(p.seq_lens + b);
+    if (L < 1 || L > kBlock * p.max_blocks) return false;
+    const int nb = (L + kBlock - 1) / kBlock;
+    if (nb <= p.top_k) return false;
+    const int h0 = hr * HS;
+    d = Desc{kDescSelect, 0, 0, b, h0, nb - 1, min(HS, H - h0), L};
+    return true;
+  }
+  const int a = item - p.n_score_items - p.n_select_items;
+  const int row = a / p.splits_per_row, split = a % p.splits_per_row;
+  const int L = __ldg(p.seq_lens + row / H);
+  if (L < 1 || L > kBlock * p.max_blocks) {
+    if (split != 0) return false;
+    d = Desc{kDescEmptyRow, 0, 0, row, 0, 1, 0, L};
+    return true;
   }
   const int nb = (L + kBlock - 1) / kBlock;
   const bool every_block = p.top_k == 0 || nb <= p.top_k;
-  if (p.top_k > 0 && nb <= p.top_k && split == 0) {
-    // no selection ran for this row: its kept list is every block, -1 padded
-    for (int i = tid; i < p.top_k; i += kThreads) srow_w[i] = i < nb ? i : -1;
-  }
   const int n_items = p.top_k == 0 ? nb : min(nb, p.top_k);
   const int splits = (n_items + p.items_per_split - 1) / p.items_per_split;
-  if (split >= splits) return;
-  const int i0 = split * p.items_per_split;
-  const int cnt = min(n_items, i0 + p.items_per_split) - i0;
+  if (split >= splits) return false;
+  const int cnt = min(n_items, (split + 1) * p.items_per_split) - split * p.items_per_split;
+  const int flags = (every_block ? kAttnEveryBlock : 0) |
+                    ((p.append_final != 0 && (L % kBlock) == 0 && split == splits - 1)
+                         ? kAttnAppendLast : 0);
+  d = Desc{kDescAttn, 0, cnt, row, split, splits, flags, L};
+  return true;
+}
 
-  if (!every_block) {
-    if (tid == 0) {
-      bool ok = false;
-      for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
-        if (ld_acquire(p.ready + row) != 0) {
-          ok = true;
+template <int D, int NT>
+__device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CUtensorMap *vmap,
+                         uint8_t *ring, FusedShared &sh) {
+  KIN_TRACE_DECL
+  using R = Ring<D, NT>;
+  using C = Cfg<D, NT>;
+  const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) - C::kCW;
+  const bool leader = q == 0;
+  const uint64_t policy = l2_policy_evict_first();
+  const int H = p.num_kv_heads;
+  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
+  uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
+  uint32_t nd = 0;            // descriptors read (and, by the leader, pushed)
+  int next = 0;
+  if (leader && lane == 0) next = atomicAdd(p.work_next, 1);
+
+  // Lane 0: claim the next stage of the sub-ring of consumer q + kProducers cc and post
+  // what will land there.  The j-th page (score stage) of an item in this pipeline goes
+  // to consumer cc = j % kPPC: a fixed function of the item, so that the partition of an
+  // item's pages among warps, and with it every rounding, is the same on every call.
+  auto claim = [&](int cc, int4 meta, uint32_t bytes) {
+    const uint32_t n = pos[cc];
+    const int s = R::slot(q + kProducers * cc, n);
+    KIN_TIC(t0);
+    wait_bar(&sh.empty[s], R::phase(n) ^ 1u, sh, p.err);
+    KIN_TOC(kTrPWaitEmpty, t0);
+    sh.meta[s] = meta;
+    if (bytes != 0)
+      mbar_arrive_expect_tx(&sh.full[s], bytes);
+    else
+      mbar_arrive(&sh.full[s]);
+    return s;
+  };
+
+  KIN_TIC(t_start);
+#pragma unroll 1
+  while (true) {
+    if (leader) {
+      // Next item with work (END once the queue is exhausted), pushed as a descriptor.
+      Desc d{kDescEnd, 0, 0, 0, 0, 0, 0, 0};
+      KIN_TIC(t_next);
+      while (true) {
+        const int item = __shfl_sync(0xffffffffu, next, 0);
+        if (item >= total) break;
+        if (lane == 0) next = atomicAdd(p.work_next, 1);   // prefetch the one after
+        if (make_desc<D>(p, item, d)) break;
+      }
+      KIN_TOC(kTrPNext, t_next);
+      if (lane == 0) {
+        const int slot = nd % kDescs;
+        KIN_TIC(t0);
+        wait_bar(&sh.dempty[slot], ((nd / kDescs) & 1u) ^ 1u, sh, p.err);
+        KIN_TOC(kTrPPush, t0);
+        sh.desc[slot] = d;
+        mbar_arrive(&sh.dfull[slot]);
+      }
+      __syncwarp();
+    }
+    const int slot = nd % kDescs;
+    if (!wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err)) break;
+    const Desc d = sh.desc[slot];
+    ++nd;
+    if (d.kind == kDescScore) {
+      // Ring stages t = q, q + kProducers, ... of the chunk: pps pages' centroid rows each.
+      const int b = d.row, h0 = d.x0, j0 = d.x1, hs = d.x2, L = d.x3;
+      const int npg = min((L + kBlock - 1) / kBlock - 1, j0 + p.score_chunk) - j0;
+      const int pps = R::kStageBytes / (hs * D * 2);
+      const uint32_t row_bytes = static_cast<uint32_t>(hs) * D * 2;
+      int *plist = sh.plist[q];
+      const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks + j0;
+      KIN_TIC(t_meta);
+      for (int i = lane; i < npg; i += 32) {
+        int pg = __ldg(trow + i);
+        if (pg < 0 || pg >= p.num_pages) {
+          if (q == 0) flag_error(p.err, KIN_DEVERR_PAGE_ID);
+          pg = -1;
+        }
+        plist[i] = pg;
+      }
+      __syncwarp();
+      KIN_TOC(kTrPMeta, t_meta);
+      for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
+        KIN_TIC(t_issue);
+        const int cc = j % C::kPPC;
+        const int pa = t * pps, pb = min(npg, pa + pps);
+        const int pg = lane < pb - pa ? plist[pa + lane] : -1;
+        const uint32_t vmask = __ballot_sync(0xffffffffu, pg >= 0);
+        int s = 0;
+        if (lane == 0)
+          s = claim(cc, make_int4(j0 + pa, pb - pa, static_cast<int>(vmask), 0), __popc(vmask) * row_bytes);
+        s = __shfl_sync(0xffffffffu, s, 0);
+        ++pos[cc];
+        if (pg >= 0)
+          bulk_load(ring + s * R::kStageBytes + lane * row_bytes,
+                    p.centroids + (static_cast<int64_t>(pg) * H + h0) * D, row_bytes, &sh.full[s],
+                    policy);
+        KIN_TOC(kTrPIssue, t_issue);
+      }
+    } else if (d.kind == kDescAttn) {
+      // Pages i = q, q + kProducers, ... of the split: lane l reads page
+      // i = base + l * kProducers, then the pages are staged in order.
+      const int row = d.row, L = d.x3, cnt = d.count;
+      const int b = row / H;
+      const int nb = (L + kBlock - 1) / kBlock;
+      const bool every_block = (d.x2 & kAttnEveryBlock) != 0;
+      const int i0 = d.x0 * p.items_per_split;
+      if (!every_block && q < cnt) {
+        KIN_TIC(t0);
+        if (lane == 0) wait_flag(p.ready + row, 1, sh, p.err);
+        __syncwarp();
+        KIN_TOC(kTrPReady, t0);
+      }
+      const int32_t *srow = p.sel + static_cast<int64_t>(row) * p.top_k;
+      const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+      const int32_t ybase = (row % H) * kBlock;
+      for (int base = q; base < cnt; base += 32 * kProducers) {
+        KIN_TIC(t_meta);
+        const int i = base + lane * kProducers;
+        int page = -1, ntok = 0;
+        if (i < cnt) {
+          const int j = every_block ? i0 + i : __ldcg(srow + i0 + i);
+          if (j >= 0 && j < nb) {
+            const int pg = __ldg(trow + j);
+            if (pg >= 0 && pg < p.num_pages) {
+              page = pg;
+              ntok = min(kBlock, L - kBlock * j);
+            } else {
+              flag_error(p.err, KIN_DEVERR_PAGE_ID);
+            }
+          }
+        }
+        KIN_TOC(kTrPMeta, t_meta);
+        const int n_here = min(32, (cnt - base + kProducers - 1) / kProducers);
+        for (int l = 0; l < n_here; ++l) {
+          KIN_TIC(t_issue);
+          const int pg = __shfl_sync(0xffffffffu, page, l);
+          const int nt = __shfl_sync(0xffffffffu, ntok, l);
+          int s = 0;
+          const int cc = ((base - q) / kProducers + l) % C::kPPC;
+          if (lane == 0) s = claim(cc, make_int4(pg, nt, 0, 0), pg >= 0 ? R::kStageBytes : 0u);
+          s = __shfl_sync(0xffffffffu, s, 0);
+          ++pos[cc];
+          if (pg >= 0 && lane < 2) {   // lane 0: K, lane 1: V; one copy per page each
+            uint8_t *dst = ring + s * R::kStageBytes + (lane ? BfTile<D>::kKBytes : 0);
+            const CUtensorMap *map = lane ? vmap : kmap;
+            if (D == 128)
+              tma_load_3d(dst, map, 0, pg * H * kBlock + ybase, 0, &sh.full[s], policy);
+            else
+              tma_load_2d(dst, map, 0, pg * H * kBlock + ybase, &sh.full[s], policy);
+          }
+          KIN_TOC(kTrPIssue, t_issue);
+          KIN_COUNT(kTrPPages, 1);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.dempty[slot]);
+    if (d.kind == kDescEnd) break;
+    KIN_COUNT(kTrPItems, 1);
+  }
+  KIN_TOC(kTrTotal, t_start);
+  KIN_TRACE_FLUSH;
+  // Leave no copy in flight: wait (bounded) for the last use of each stage of the sub-rings
+  // this warp fills.  Their consumers normally saw them all complete; this matters only
+  // after a timeout.
+  if (lane == 0) {
+    for (int cc = 0; cc < C::kPPC; ++cc) {
+      const uint32_t n = pos[cc];
+      for (uint32_t j = 0; j < static_cast<uint32_t>(R::kPer) && j < n; ++j) {
+        const uint32_t last = j + ((n - 1 - j) / R::kPer) * R::kPer;
+        if (!mbar_wait(&sh.full[R::slot(q + kProducers * cc, last)], R::phase(last))) {
+          flag_error(p.err, KIN_DEVERR_TIMEOUT);
           break;
         }
-        __nanosleep(128);
-      }
-      if (!ok) flag_error(p.err, KIN_DEVERR_TIMEOUT);
-    }
-    __syncthreads();
-  }
-  const int32_t *srow = p.sel + static_cast<int64_t>(row) * p.top_k;
-  for (int i = tid; i < cnt; i += kThreads) {
-    const int j = every_block ? i0 + i : __ldcg(srow + i0 + i);
-    int page = -1, ntok = 0;
-    if (j >= 0 && j < nb) {
-      const int pg = __ldg(p.block_table + static_cast<int64_t>(b) * p.max_blocks + j);
-      if (pg >= 0 && pg < p.num_pages) {
-        page = pg;
-        ntok = min(kBlock, L - kBlock * j);
-      } else {
-        flag_error(p.err, KIN_DEVERR_PAGE_ID);
       }
     }
-    sh.page[i] = page;
-    sh.ntok[i] = ntok;
   }
-  __syncthreads();
+  __syncwarp();
+}
 
-  const int my_cnt = cnt > warp ? (cnt - warp + kWarps - 1) / kWarps : 0;
-  uint8_t *wbase = smem + warp * kStages * Tile::kStageBytes;
-  uint64_t *wbar = sh.bars + warp * kStages;
-  const int32_t ybase = h * kBlock;
-  auto issue = [&](int n) {   // lane 0: stage the warp's n-th block of this item
-    const uint32_t u = uses + n;
-    const int s = u % kStages;
-    const int page = sh.page[warp + n * kWarps];
-    if (page < 0) {
-      mbar_arrive(&wbar[s]);
-      return;
+// ----------------------------------------------------------------------------------
+// Consumer warps (threads 0 .. 32 kCW - 1; Cfg::Bar syncs exactly them).  Consumer warp w
+// belongs to pipeline q = w % kProducers as its c = w / kProducers-th consumer: of the
+// pipeline's pages (score stages) j = 0, 1, ... of an item it takes those with
+// j % kPPC == c, and finds them at its own sub-ring position n.
+// ----------------------------------------------------------------------------------
+template <int D, int NT>
+__device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring, float *qsum,
+                              FusedShared &sh, uint32_t &n KIN_TRACE_PARAM) {
+  using R = Ring<D, NT>;
+  using C = Cfg<D, NT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = warp % kProducers, c = warp / kProducers;
+  const int H = p.num_kv_heads, G = p.group;
+  const int b = d.row, h0 = d.x0, hs = d.x2;
+  // Group-summed queries of the range's heads: fp32, summed over g in order.  One thread
+  // per 8 consecutive dimensions of one head (16-byte loads).
+  KIN_TIC(t_q);
+  for (int x = tid; x < hs * (D / 8); x += C::kCThreads) {
+    const int hh = x / (D / 8), c8 = (x % (D / 8)) * 8;
+    const __nv_bfloat16 *qp = p.q + (static_cast<int64_t>(b) * H * G + (h0 + hh) * G) * D + c8;
+    float acc[8], f[8];
+    Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp)), acc);
+    for (int g = 1; g < G; ++g) {
+      Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp + g * D)), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += f[i];
     }
-    uint8_t *dst = wbase + s * Tile::kStageBytes;
-    mbar_arrive_expect_tx(&wbar[s], Tile::kStageBytes);
-    const int32_t y = page * H * kBlock + ybase;
-#pragma unroll
-    for (int x = 0; x < Tile::kBoxes; ++x)
-      tma_load_2d(dst + x * Tile::kBoxBytes, kmap, x * Tile::kBoxCols, y, &wbar[s], policy);
-#pragma unroll
-    for (int x = 0; x < Tile::kBoxes; ++x)
-      tma_load_2d(dst + Tile::kKBytes + x * Tile::kBoxBytes, vmap, x * Tile::kBoxCols, y,
-                  &wbar[s], policy);
-  };
-  if (lane == 0) {
-    fence_proxy_async_smem();
-    for (int n = 0; n < kStages && n < my_cnt; ++n) issue(n);
+    float4 *dst = reinterpret_cast<float4 *>(qsum + hh * D + c8);
+    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
   }
-  uint32_t qa[D / 16][4];
-  load_q_frags<D>(qa, p.q + (static_cast<int64_t>(b) * H * G + h * G) * D, G, lane);
+  C::Bar::sync();
+  KIN_TOC(kTrCScoreQ, t_q);
+  // A stage holds at most 32 centroids ([pages][heads][d]).  Lane l owns dimensions
+  // [l * kPer, l * kPer + kPer) of every centroid (conflict-free shared reads); the 32
+  // partial sums are then reduced across lanes by a butterfly that leaves centroid c's
+  // score in lane c.
+  constexpr int kPer = D / 32;
+  for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
+    if (j % C::kPPC != c) continue;
+    const int s = R::slot(warp, n);
+    KIN_TIC(t_w);
+    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
+    ++n;
+    KIN_TOC(kTrCScoreWait, t_w);
+    KIN_TIC(t_sc);
+    const int4 meta = sh.meta[s];
+    const int jst = meta.x, np = meta.y;
+    const uint32_t vmask = static_cast<uint32_t>(meta.z);
+    const uint8_t *stage = ring + s * R::kStageBytes + lane * kPer * 2;
+    const float *qs = qsum + lane * kPer;
+    const int nc = ok ? np * hs : 0;
+    // Every load is unconditional (stale shared memory is harmless) so that the unrolled
+    // loop issues them back to back; invalid centroids are masked after the products.
+    float v[32];
+    int hh = 0, pi = 0;
+#pragma unroll
+    for (int cc = 0; cc < 32; ++cc) {
+      float f[kPer], qv[kPer];
+      if constexpr (kPer == 4) {
+        const uint2 raw = *reinterpret_cast<const uint2 *>(stage + cc * (D * 2));
+        f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
+        const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * D);
+        qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+      } else {
+        const uint32_t raw = *reinterpret_cast<const uint32_t *>(stage + cc * (D * 2));
+        f[0] = bf16_lo(raw); f[1] = bf16_hi(raw);
+        const float2 q2 = *reinterpret_cast<const float2 *>(qs + hh * D);
+        qv[0] = q2.x; qv[1] = q2.y;
+      }
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) acc = fmaf(qv[i], f[i], acc);
+      v[cc] = (cc < nc && ((vmask >> pi) & 1u)) ? acc : 0.f;
+      if (++hh == hs) {
+        hh = 0;
+        ++pi;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < o; ++k) {
+        const float send = upper ? v[k] : v[k + o];
+        const float keep = upper ? v[k + o] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    if (lane < nc) {
+      const int pl = lane / hs, hl = lane % hs;
+      __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
+             ((vmask >> pl) & 1u) ? v[0] : -INFINITY);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+    KIN_TOC(kTrCScoreComp, t_sc);
+  }
+  // Publish the item: the barrier orders every warp's score stores before the release.
+  C::Bar::sync();
+  if (tid == 0) red_add_release_gpu(p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range, 1);
+}
+
+template <int D, int NT>
+__device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scratch,
+                               FusedShared &sh KIN_TRACE_PARAM) {
+  using C = Cfg<D, NT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int H = p.num_kv_heads;
+  const int b = d.row, h0 = d.x0, n = d.x1, hs = d.x2;
+  const int nb = n + 1;
+  KIN_TIC(t_sw);
+  if (tid == 0) {
+    // Wait until every score item of this (sequence, head range) has published.
+    const int32_t *cnt = p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range;
+    wait_flag(cnt, (n + p.score_chunk - 1) / p.score_chunk, sh, p.err);
+  }
+  C::Bar::sync();
+  KIN_TOC(kTrCSelWait, t_sw);
+  int *hist = reinterpret_cast<int *>(scratch) + warp * 256;
+  KIN_TIC(t_sel);
+  for (int hh = warp; hh < hs; hh += C::kCW) {
+    const int row = b * H + h0 + hh;
+    const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
+    int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
+    if (n <= 32 * 16)
+      warp_select_reg<16>(srow, n, p.top_k - 1, nb, hist, out, lane);
+    else if (n <= 32 * 64)
+      warp_select_reg<64>(srow, n, p.top_k - 1, nb, hist, out, lane);
+    else
+      warp_select(srow, n, p.top_k - 1, nb, nullptr, hist, out, lane);
+    __syncwarp();
+    if (lane == 0) st_release_gpu(p.ready + row, 1);
+    __syncwarp();
+  }
+  KIN_TOC(kTrCSelComp, t_sel);
+  C::Bar::sync();   // the scratch is reused by the next item
+}
+
+template <int D, int NT>
+__device__ void consume_attention(const FusedParams &p, const Desc &d, uint8_t *ring,
+                                  uint8_t *scratch, FusedShared &sh,
+                                  uint32_t &n KIN_TRACE_PARAM) {
+  using R = Ring<D, NT>;
+  using Tile = BfTile<D>;
+  using C = Cfg<D, NT>;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int q = warp % kProducers, c = warp / kProducers;
+  const int H = p.num_kv_heads, G = p.group;
+  const int row = d.row, split = d.x0, splits = d.x1, flags = d.x2, L = d.x3, cnt = d.count;
+  const int b = row / H, h = row % H;
+  const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, G, H};
+  if (p.top_k > 0 && (flags & kAttnEveryBlock) && split == 0) {
+    // no selection ran for this row: its kept list is every block, -1 padded
+    const int nb = (L + kBlock - 1) / kBlock;
+    int32_t *srow = p.sel + static_cast<int64_t>(row) * p.top_k;
+    for (int i = tid; i < p.top_k; i += C::kCThreads) srow[i] = i < nb ? i : -1;
+  }
+  KIN_TIC(t_q);
+  uint32_t qb[D / 16][NT][2];
+  load_qT_frags<D, NT>(qb, p.q + (static_cast<int64_t>(b) * H * G + h * G) * D, G, lane);
+  KIN_TOC(kTrCQ, t_q);
   const float scale_log2 = p.sm_scale * kLog2e;
-  const bool append = p.append_final != 0 && (L % kBlock) == 0 && split == splits - 1;
-  WarpSoftmax<D> st;
+  const bool append = (flags & kAttnAppendLast) != 0;
+  WarpSoftmaxT<D, NT> st;
   st.init();
-  for (int n = 0; n < my_cnt; ++n) {
-    const uint32_t u = uses + n;
-    const int s = u % kStages;
-    const int it = warp + n * kWarps;
-    const int ntok = sh.ntok[it];
-    if (!mbar_wait(&wbar[s], (u / kStages) & 1)) {
-      if (lane == 0) flag_error(p.err, KIN_DEVERR_TIMEOUT);
-    } else if (ntok > 0) {
-      uint8_t *stage = wbase + s * Tile::kStageBytes;
+  for (int i = q, j = 0; i < cnt; i += kProducers, ++j) {
+    if (j % C::kPPC != c) continue;
+    const int s = R::slot(warp, n);
+    KIN_TIC(t_w);
+    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
+    ++n;
+    KIN_TOC(kTrCWaitFull, t_w);
+    KIN_TIC(t_pg);
+    const int4 meta = sh.meta[s];
+    const int page = meta.x, ntok = meta.y;
+    bool wrote = false;
+    if (ok && ntok > 0) {
+      uint8_t *stage = ring + s * R::kStageBytes;
       if (ntok < kBlock) {
         // Stale slots of a partial final page may hold anything (even NaN): zero their
         // V rows so that P = 0 times V stays 0.
@@ -339,86 +795,135 @@ __device__ void attention_item(const FusedParams &p, const CUtensorMap *kmap,
           *reinterpret_cast<uint4 *>(vrow + (rem / 8) * Tile::kBoxBytes + t * 128 + (rem % 8) * 16) =
               make_uint4(0, 0, 0, 0);
         }
+        wrote = true;
         __syncwarp();
-      } else if (append && it == cnt - 1) {
+      } else if (append && i == cnt - 1) {
         // The final block just became complete: its centroid (fp32 sum over the 16
         // tokens in order, times 1/16, rounded to bf16) from the staged keys.
         constexpr int kPer = D / 32;
         float acc[kPer];
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) acc[i] = 0.f;
+        for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
 #pragma unroll
         for (int t = 0; t < kBlock; ++t) {
           const uint8_t *src = stage + swz_offset(t, lane * kPer);
 #pragma unroll
-          for (int i = 0; i < kPer; ++i) {
-            const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[i]);
-            acc[i] = t == 0 ? x : __fadd_rn(acc[i], x);
+          for (int k = 0; k < kPer; ++k) {
+            const float x = __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(src)[k]);
+            acc[k] = t == 0 ? x : __fadd_rn(acc[k], x);
           }
         }
-        __nv_bfloat16 *dst = p.cent_out + (static_cast<int64_t>(sh.page[it]) * H + h) * D + lane * kPer;
+        __nv_bfloat16 *dst = p.cent_out + (static_cast<int64_t>(page) * H + h) * D + lane * kPer;
 #pragma unroll
-        for (int i = 0; i < kPer; ++i) dst[i] = __float2bfloat16_rn(__fmul_rn(acc[i], 1.0f / kBlock));
+        for (int k = 0; k < kPer; ++k) dst[k] = __float2bfloat16_rn(__fmul_rn(acc[k], 1.0f / kBlock));
       }
       const uint32_t sK = smem_u32(stage);
-      st.page(qa, sK, sK + Tile::kKBytes, ntok, scale_log2, lane);
+      st.page(qb, sK, sK + Tile::kKBytes, ntok, scale_log2, lane);
     }
+    // generic-proxy writes to the stage must be ordered before the next TMA into it
+    if (wrote) fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && n + kStages < my_cnt) {
-      fence_proxy_async_smem();
-      issue(n + kStages);
-    }
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+    KIN_TOC(kTrCPage, t_pg);
+    KIN_COUNT(kTrCPages, 1);
   }
-  uses += my_cnt;
-  __syncthreads();   // every stage consumed: reuse the stage memory for the combine
-  float *wm = reinterpret_cast<float *>(smem);
-  float *wl = wm + kWarps * kMaxGroup;
-  float *wo = wl + kWarps * kMaxGroup;
-  st.store(wm, wl, wo, warp, lane);
-  __syncthreads();
-  combine_and_emit<__nv_bfloat16, D>(ec, row, b, h, split, splits, wm, wl, wo, &sh.flag);
-  fence_proxy_async_smem();   // the combine buffers are overwritten by the next copies
-  __syncthreads();
+  KIN_TIC(t_ep);
+  float *wm = reinterpret_cast<float *>(scratch);
+  float *wl = wm + C::kCW * C::kQMax;
+  float *wo = wl + C::kCW * C::kQMax;
+  C::Bar::sync();   // the scratch may still hold the previous item's data
+  KIN_TOC(kTrCEpiBar, t_ep);
+  st.store(wm + warp * C::kQMax, wl + warp * C::kQMax, wo + warp * C::kQMax * D, lane, G);
+  C::Bar::sync();
+  combine_and_emit<__nv_bfloat16, D, C::kCW, C::kQMax, C::kCThreads, typename C::Bar>(
+      ec, row, b, h, split, splits, wm, wl, wo, &sh.flag);
+  KIN_TOC(kTrCEpilogue, t_ep);
 }
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 3)
+template <int D, int NT>
+__device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch, FusedShared &sh) {
+  using C = Cfg<D, NT>;
+  KIN_TRACE_DECL
+  uint32_t n = 0;   // this warp's own pages / score stages so far (its sub-ring position)
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t nd = 0;
+  KIN_TIC(t_start);
+#pragma unroll 1
+  while (true) {
+    const int slot = nd % kDescs;
+    KIN_TIC(t_d);
+    const bool got = wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err);
+    KIN_TOC(kTrCDesc, t_d);
+    if (!got) break;
+    const Desc d = sh.desc[slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.dempty[slot]);
+    ++nd;
+    if (d.kind == kDescEnd) break;
+    KIN_COUNT(kTrCItems, 1);
+    if (d.kind == kDescScore) {
+      KIN_TIC(t0);
+      consume_score<D, NT>(p, d, ring, reinterpret_cast<float *>(scratch), sh, n KIN_TRACE_ARG);
+      KIN_TOC(kTrCScore, t0);
+    } else if (d.kind == kDescSelect) {
+      KIN_TIC(t0);
+      consume_select<D, NT>(p, d, scratch, sh KIN_TRACE_ARG);
+      KIN_TOC(kTrCSelect, t0);
+    } else if (d.kind == kDescAttn) {
+      consume_attention<D, NT>(p, d, ring, scratch, sh, n KIN_TRACE_ARG);
+    } else {   // kDescEmptyRow: a sequence whose length is out of range
+      const int H = p.num_kv_heads;
+      const int b = d.row / H, h = d.row % H;
+      const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, p.group, H};
+      write_empty_row<__nv_bfloat16, D, C::kCThreads>(ec, b, h);
+      if (tid == 0 && h == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
+      if (p.top_k > 0) {
+        int32_t *srow = p.sel + static_cast<int64_t>(d.row) * p.top_k;
+        for (int i = tid; i < p.top_k; i += C::kCThreads) srow[i] = -1;
+      }
+    }
+  }
+  KIN_TOC(kTrTotal, t_start);
+  KIN_TRACE_FLUSH;
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(Cfg<D, NT>::kAllThreads, 1)
     fused_decode_kernel(const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap, const FusedParams p) {
+  using C = Cfg<D, NT>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
-  uint8_t *smem = align1024(smem_raw);
+  __shared__ FusedShared sh;
+  uint8_t *ring = align1024(smem_raw);
+  uint8_t *scratch = ring + Ring<D, NT>::kBytes;
   const int tid = threadIdx.x;
-  if (tid < kWarps * kStages) mbar_init(&sh.bars[tid], 1);
-  fence_mbar_init();
-  if (tid == 0) sh.next = atomicAdd(p.work_next, 1);
-  __syncthreads();
-  const uint64_t policy = l2_policy_evict_first();
-  uint32_t uses = 0;
-  const int total = p.n_score_items + p.n_attn_items;
-  while (true) {
-    const int item = sh.next;
-    __syncthreads();
-    if (item >= total) break;
-    int next = 0;
-    if (tid == 0) next = atomicAdd(p.work_next, 1);   // consumed at the end of the item
-    if (item < p.n_score_items)
-      score_item<D>(p, item, smem, sh);
-    else
-      attention_item<D>(p, &kmap, &vmap, item - p.n_score_items, smem, sh, uses, policy);
-    if (tid == 0) sh.next = next;
-    __syncthreads();
+  if (tid == 0) {
+    for (int s = 0; s < Ring<D, NT>::kStages; ++s) {
+      mbar_init(&sh.full[s], 1);
+      mbar_init(&sh.empty[s], 1);
+    }
+    for (int i = 0; i < kDescs; ++i) {
+      mbar_init(&sh.dfull[i], 1);
+      mbar_init(&sh.dempty[i], C::kCW + kProducers);
+    }
+    sh.abort = 0;
+    fence_mbar_init();
   }
+  __syncthreads();
+  if ((tid >> 5) >= C::kCW)
+    producer<D, NT>(p, &kmap, &vmap, ring, sh);
+  else
+    consumer<D, NT>(p, ring, scratch, sh);
 }
 
-template <int D>
+template <int D, int NT>
 cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtensorMap *vmap,
                      cudaStream_t stream) {
-  static_assert(fused_smem_bytes<D>() >= combine_smem_bytes(D), "combine must fit");
-  const size_t smem = fused_smem_bytes<D>() + 1024;
+  using C = Cfg<D, NT>;
+  const size_t smem = fused_smem_bytes<D, NT>();
   static int occupancy = 0, sms = 0;
   if (occupancy == 0) {
-    cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<D, NT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -427,26 +932,40 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, fused_decode_kernel<D>,
-                                                      kThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, fused_decode_kernel<D, NT>,
+                                                      C::kAllThreads, smem);
     if (e != cudaSuccess) return e;
     if (occupancy < 1) occupancy = 1;
   }
-  const int total = p.n_score_items + p.n_attn_items;
+  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
   const int grid = min(total, sms * occupancy);
   if (grid <= 0) return cudaSuccess;
-  fused_decode_kernel<D><<<grid, kThreads, smem, stream>>>(*kmap, *vmap, p);
+  fused_decode_kernel<D, NT><<<grid, C::kAllThreads, smem, stream>>>(*kmap, *vmap, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-int fused_chunk() { return kChunk; }
+int fused_max_score_chunk() { return kMaxScoreChunk; }
+
+#ifdef KIN_TRACE_CYCLES
+// Copy out (and clear) the cycle counters: [CTA][warp][slot], 160 x 12 x 16 words.
+cudaError_t trace_take(unsigned long long *host, size_t words) {
+  const size_t n = sizeof(g_trace) / sizeof(g_trace[0]);
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_trace, (words < n ? words : n) * 8);
+  if (e != cudaSuccess) return e;
+  static unsigned long long zeros[sizeof(g_trace) / sizeof(g_trace[0])];
+  return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros));
+}
+#endif
 
 cudaError_t launch_fused(int head_dim, const FusedParams &p, const CUtensorMap *kmap,
                          const CUtensorMap *vmap, cudaStream_t stream) {
-  return head_dim == 128 ? launch_d<128>(p, kmap, vmap, stream)
-                         : launch_d<64>(p, kmap, vmap, stream);
+  if (p.group <= 8)
+    return head_dim == 128 ? launch_d<128, 1>(p, kmap, vmap, stream)
+                           : launch_d<64, 1>(p, kmap, vmap, stream);
+  return head_dim == 128 ? launch_d<128, 2>(p, kmap, vmap, stream)
+                         : launch_d<64, 2>(p, kmap, vmap, stream);
 }
 
 }  // namespace kin

@@ -31,17 +31,23 @@ kin_status cuda_fail(cudaError_t e, const char *what) {
 }
 
 // Split planning is a pure function of the shapes (never of the device), so the
-// workspace size and the launch always agree.  It targets about two waves of
-// attention CTAs over the 148 SMs of a B300 at three resident CTAs per SM.
+// workspace size and the launch always agree.  The bf16 kernel runs one CTA per SM of a
+// B300 (148); the plan aims at about three attention items and three score items per CTA:
+// enough for the work queue to balance, few enough that per-item costs stay small.
 constexpr int kPlanSMs = 148;
-constexpr int kPlanCtasPerSM = 3;
-constexpr int kMaxItemsPerSplit = 64;
+#ifndef KIN_PLAN_ATTN_ITEMS
+#define KIN_PLAN_ATTN_ITEMS 3
+#endif
+constexpr int kAttnItemsPerCta = KIN_PLAN_ATTN_ITEMS;
+constexpr int kScoreItemsPerCta = 3;
+constexpr int kMaxItemsPerSplit = 256;
 constexpr int kMaxBlocksLimit = 16384;
+constexpr int kHeadsPerRange = 32;
 
 struct Plan {
   int rows, group, max_items, items_per_split, max_splits;
-  int score_chunk;      // fp32 standalone score kernel: candidates per CTA
-  int chunks_per_row;   // bf16 fused kernel: score items per row
+  int score_chunk;      // candidate blocks per score CTA (fp32) or score item (bf16)
+  int heads_per_range, head_ranges, chunks_per_seq;   // bf16 score / select items
 };
 
 Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
@@ -50,9 +56,7 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   pl.group = a->num_q_heads / c->num_kv_heads;
   pl.max_items = mode == 0 ? (a->top_k < a->max_blocks ? a->top_k : a->max_blocks) : a->max_blocks;
   const int warps = attention_warps();
-  // About four attention work items per resident CTA: enough for the work queue (bf16)
-  // or the wave tail (fp32) to balance, few enough that the per-item start-up is small.
-  const int target = kPlanSMs * kPlanCtasPerSM * 4;
+  const int target = kPlanSMs * kAttnItemsPerCta;
   int splits = (target + pl.rows - 1) / pl.rows;
   const int max_useful = (pl.max_items + 2 * warps - 1) / (2 * warps);  // >= 2 blocks per warp
   if (splits > max_useful) splits = max_useful;
@@ -62,24 +66,50 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   if (ips > kMaxItemsPerSplit) ips = kMaxItemsPerSplit;
   pl.items_per_split = ips;
   pl.max_splits = (pl.max_items + ips - 1) / ips;
-  // fp32 score kernel: about 8 CTAs per SM over all candidate blocks, 64..1024 per CTA.
-  const long long cand = static_cast<long long>(pl.rows) * a->max_blocks;
-  long long chunk = (cand + kPlanSMs * 8 - 1) / (kPlanSMs * 8);
-  chunk = (chunk + 63) / 64 * 64;
-  if (chunk < 64) chunk = 64;
-  if (chunk > 1024) chunk = 1024;
-  pl.score_chunk = static_cast<int>(chunk);
-  pl.chunks_per_row = mode == 0 ? (a->max_blocks - 1 + fused_chunk() - 1) / fused_chunk() : 0;
+  pl.heads_per_range = c->num_kv_heads < kHeadsPerRange ? c->num_kv_heads : kHeadsPerRange;
+  pl.head_ranges = (c->num_kv_heads + pl.heads_per_range - 1) / pl.heads_per_range;
+  if (c->dtype == KIN_BF16) {
+    // Score items: chunks of the candidate blocks (all but the final block) of one
+    // (sequence, head range), a multiple of the pages one ring stage holds.
+    const int pps = 32 / pl.heads_per_range;
+    const long long cand = static_cast<long long>(a->batch) * pl.head_ranges * (a->max_blocks - 1);
+    long long chunk = (cand + kPlanSMs * kScoreItemsPerCta - 1) / (kPlanSMs * kScoreItemsPerCta);
+    if (chunk < 2 * pps) chunk = 2 * pps;
+    chunk = (chunk + pps - 1) / pps * pps;
+    const int cap = fused_max_score_chunk() / pps * pps;
+    if (chunk > cap) chunk = cap;
+    pl.score_chunk = static_cast<int>(chunk);
+    const int n = a->max_blocks - 1;
+    pl.chunks_per_seq = mode == 0 && n > 0 ? (n + pl.score_chunk - 1) / pl.score_chunk : 0;
+  } else {
+    // fp32 score kernel: about 8 CTAs per SM over all candidate blocks, 64..1024 per CTA.
+    const long long cand = static_cast<long long>(pl.rows) * a->max_blocks;
+    long long chunk = (cand + kPlanSMs * 8 - 1) / (kPlanSMs * 8);
+    chunk = (chunk + 63) / 64 * 64;
+    if (chunk < 64) chunk = 64;
+    if (chunk > 1024) chunk = 1024;
+    pl.score_chunk = static_cast<int>(chunk);
+  }
   return pl;
 }
 
-// Arrival counters, ready flags and the work-queue head: cleared by every decode call.
-size_t counter_bytes(const Plan &pl) {
-  return sizeof(int32_t) * (3 * static_cast<size_t>(pl.rows) + 1);
+// Counters cleared by every decode call: the work-queue head, score arrivals per
+// (sequence, head range), split arrivals and ready flags per row.
+struct Counters {
+  size_t work_next, score_cnt, attn_cnt, ready, count;
+};
+Counters counter_layout(const kin_decode_args *a, const Plan &pl) {
+  Counters k{};
+  k.work_next = 0;
+  k.score_cnt = 1;
+  k.attn_cnt = k.score_cnt + static_cast<size_t>(a->batch) * pl.head_ranges;
+  k.ready = k.attn_cnt + pl.rows;
+  k.count = k.ready + pl.rows;
+  return k;
 }
 
 struct Layout {
-  size_t counters, part_ml, part_o, scores, sel, total;
+  size_t counters, counter_bytes, part_ml, part_o, scores, sel, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -87,8 +117,9 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &pl, int mode) {
   Layout L{};
   size_t off = 0;
-  L.counters = off;   // score_cnt[rows], attn_cnt[rows], ready[rows], work_next
-  off = align256(off + counter_bytes(pl));
+  L.counters = off;
+  L.counter_bytes = sizeof(int32_t) * counter_layout(a, pl).count;
+  off = align256(off + L.counter_bytes);
   L.part_ml = off;
   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group);
   L.part_o = off;
@@ -185,19 +216,34 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// View the page pool as a 2-D bf16 tensor [P*H*16 rows, d columns] and move 64-column
-// by 16-row boxes (one page of one head) with the 128-byte swizzle.
+// The page pool as a bf16 tensor of P*H*16 rows of d columns, copied one page of one head
+// (16 rows) per TMA with the 128-byte swizzle: rows are split into 64-column halves of
+// 128 bytes, and a page lands in shared memory as [d/64 halves][16 rows][64 columns].
+// d = 64: a 2-D view (64 columns, rows), box {64, 16}.  d = 128: a 3-D view (64 columns,
+// rows, 2 halves) with strides (256 B, 128 B), box {64, 16, 2}, so one copy moves the
+// whole page in that same layout.
 kin_status encode_page_map(CUtensorMap *map, const kin_kv_cache *c, const void *base) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return fail(KIN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(c->head_dim),
-                              static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * kBlock};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(c->head_dim) * 2};
-  const cuuint32_t box[2] = {64, kBlock};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint64_t rows = static_cast<cuuint64_t>(c->num_pages) * c->num_kv_heads * kBlock;
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(c->head_dim) * 2;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r;
+  if (c->head_dim == 128) {
+    const cuuint64_t dims[3] = {64, rows, 2};
+    const cuuint64_t strides[2] = {row_bytes, 128};
+    const cuuint32_t box[3] = {64, kBlock, 2};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {64, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {64, kBlock};
+    r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+           estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
   if (r != CUDA_SUCCESS) return fail(KIN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return KIN_OK;
 }
@@ -220,9 +266,17 @@ kin_status use_device_of(const void *ptr) {
   return KIN_OK;
 }
 
+// Inside a stream capture the events become event-record nodes of the graph, so that a
+// replayed graph still timestamps its kernels.
 kin_status record(void *const *events, int i, cudaStream_t stream) {
   if (events == nullptr) return KIN_OK;
-  cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(events[i]), stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  cudaEvent_t ev = static_cast<cudaEvent_t>(events[i]);
+  e = cs == cudaStreamCaptureStatusActive
+          ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+          : cudaEventRecord(ev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return KIN_OK;
 }
@@ -244,12 +298,13 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   if (s != KIN_OK) return s;
   uint8_t *ws = static_cast<uint8_t *>(a->workspace);
   int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.counters);
+  const Counters ck = counter_layout(a, pl);
   float *scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
   int32_t *sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
   const int append = (a->flags & KIN_DECODE_APPEND_FINAL) != 0;
   if ((s = record(events, 0, stream)) != KIN_OK) return s;
   // The workspace is scratch shared with calls of other shapes: clear the counters.
-  cudaError_t me = cudaMemsetAsync(cnt, 0, counter_bytes(pl), stream);
+  cudaError_t me = cudaMemsetAsync(cnt, 0, L.counter_bytes, stream);
   if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync of the workspace counters");
 
   if (c->dtype == KIN_BF16) {
@@ -270,10 +325,10 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.sel = sel;
     fp.part_o = reinterpret_cast<float *>(ws + L.part_o);
     fp.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
-    fp.score_cnt = cnt;
-    fp.attn_cnt = cnt + pl.rows;
-    fp.ready = cnt + 2 * pl.rows;
-    fp.work_next = cnt + 3 * pl.rows;
+    fp.work_next = cnt + ck.work_next;
+    fp.score_cnt = cnt + ck.score_cnt;
+    fp.attn_cnt = cnt + ck.attn_cnt;
+    fp.ready = cnt + ck.ready;
     fp.err = a->err_flag;
     fp.num_pages = c->num_pages;
     fp.batch = a->batch;
@@ -281,10 +336,14 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.group = pl.group;
     fp.max_blocks = a->max_blocks;
     fp.top_k = mode == 0 ? a->top_k : 0;
-    fp.chunks_per_row = pl.chunks_per_row;
+    fp.heads_per_range = pl.heads_per_range;
+    fp.head_ranges = pl.head_ranges;
+    fp.score_chunk = pl.score_chunk;
+    fp.chunks_per_seq = pl.chunks_per_seq;
     fp.items_per_split = pl.items_per_split;
     fp.splits_per_row = pl.max_splits;
-    fp.n_score_items = mode == 0 ? pl.rows * pl.chunks_per_row : 0;
+    fp.n_score_items = mode == 0 ? a->batch * pl.head_ranges * pl.chunks_per_seq : 0;
+    fp.n_select_items = mode == 0 ? a->batch * pl.head_ranges : 0;
     fp.n_attn_items = pl.rows * pl.max_splits;
     fp.append_final = append;
     fp.sm_scale = a->sm_scale;
@@ -337,7 +396,7 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   ap.cent_out = a->centroids;
   ap.part_o = reinterpret_cast<float *>(ws + L.part_o);
   ap.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
-  ap.counters = cnt + pl.rows;
+  ap.counters = cnt + ck.attn_cnt;
   ap.err = a->err_flag;
   ap.num_pages = c->num_pages;
   ap.batch = a->batch;

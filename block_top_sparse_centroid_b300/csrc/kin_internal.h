@@ -56,7 +56,12 @@ struct AttnParams {
 // fp32 caches: CUDA-core split-KV attention (grid = max_splits x rows).
 cudaError_t launch_attention_f32(int head_dim, const AttnParams &p, cudaStream_t stream);
 
-// bf16 caches: one persistent kernel for score + select + attention (+ final-block append).
+// bf16 caches: one persistent, warp-specialised kernel for score + select + attention
+// (+ final-block append).  Work items, handed out in this order by a global counter:
+//   score items   (sequence b, head range hr, chunk c): scores of candidate blocks
+//                 [c * score_chunk, (c + 1) * score_chunk) for heads [hr * HS, hr * HS + HS)
+//   select items  (sequence b, head range hr): top-k selection of those rows
+//   attention     (row = b * H + h, split): attention over one split of the kept list
 struct FusedParams {
   const __nv_bfloat16 *q;          // [B, H*G, d]
   const __nv_bfloat16 *centroids;  // [P, H, d]
@@ -69,23 +74,25 @@ struct FusedParams {
   int32_t *sel;                    // [B*H, top_k]
   float *part_o;                   // [B*H, splits_per_row, G, d]
   float *part_ml;                  // [B*H, splits_per_row, G, 2]
-  int32_t *score_cnt;              // [B*H] score-chunk arrivals
+  int32_t *work_next;              // work-queue head
+  int32_t *score_cnt;              // [B * head_ranges] finished score items
   int32_t *attn_cnt;               // [B*H] split arrivals
   int32_t *ready;                  // [B*H] selection published
-  int32_t *work_next;              // work-queue head
   int32_t *err;
   int64_t num_pages;
   int batch, num_kv_heads, group, max_blocks;
   int top_k;                       // 0 = dense decode (every block, no scoring)
-  int chunks_per_row;              // score items per row
+  int heads_per_range, head_ranges;  // HS = min(H, 32) heads per score / select item
+  int score_chunk, chunks_per_seq;   // candidate blocks per score item, items per range
   int items_per_split, splits_per_row;
-  int n_score_items, n_attn_items;
+  int n_score_items, n_select_items, n_attn_items;
   int append_final;
   float sm_scale;
 };
 cudaError_t launch_fused(int head_dim, const FusedParams &p, const CUtensorMap *kmap,
                          const CUtensorMap *vmap, cudaStream_t stream);
-int fused_chunk();
+// Largest score chunk the fused kernel accepts (candidate blocks per score item).
+int fused_max_score_chunk();
 
 // Tiling facts the host needs for workspace sizing and split planning.
 int attention_warps();

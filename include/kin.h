@@ -187,7 +187,9 @@ KIN_API kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
  * kernels: events[0] before the first kernel, events[1] after scoring, events[2] after
  * selection, events[3] after attention (dense: events[1] and [2] are recorded right
  * after events[0]).  events: host array of 4 created cudaEvent_t handles.  Used to
- * time each kernel of a step without a profiler. */
+ * time each kernel of a step without a profiler.  While `stream` is being captured into
+ * a CUDA graph the records are made with cudaEventRecordExternal, so that they become
+ * event-record nodes and every replay of the graph timestamps its kernels. */
 KIN_API kin_status kin_decode_timed(const kin_kv_cache *cache, const kin_decode_args *args,
                                     int32_t mode, void *const *events, kin_stream_t stream);
 
