@@ -375,9 +375,11 @@ def main() -> int:
                      "traffic": (trec["dram_bytes_per_launch"] if trec else None)},
         "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / step_s / 1e9,
                      "frac": step_bytes / step_s / 1e9 / peak},
-        "kernels_us": {"score": statistics.mean(sp["score_ms"]) * 1e3,
-                       "select": statistics.mean(sp["sel_ms"]) * 1e3,
-                       "attention": attn_s * 1e6},
+        "kernels_us": ({"counter_memset": statistics.mean(sp["score_ms"]) * 1e3,
+                        "fused_decode_kernel": attn_s * 1e6} if cfg.dtype == "bf16" else
+                       {"score": statistics.mean(sp["score_ms"]) * 1e3,
+                        "select": statistics.mean(sp["sel_ms"]) * 1e3,
+                        "attention": attn_s * 1e6}),
         "gpu_launches": sp["launches"] + (e2e is not None) * per_step * args.steps,
         "clocks": clk,
         "e2e": e2e,

@@ -48,12 +48,14 @@ constexpr int kMaxStages = kMaxRingBytes / (64 * 64);  // stages at d = 64
 constexpr int kDescs = 8;                           // descriptor slots producer -> consumers
 constexpr int kMaxScoreChunk = 256;                 // candidate blocks per score item
 constexpr int kHeadsPerRange = 32;                  // KV heads per score / select item
+constexpr int kScoreSlots = 16;                     // score-item arrival counters (> kDescs)
 // Consumer scratch: the combine buffers of an attention item, the group-summed queries
 // of a score item, or the histograms of the selections (never at once).
 constexpr int kScratchBytes = 34 * 1024;
 static_assert(kScratchBytes >= 8 * 8 * (128 + 2) * 4, "combine buffers, 8 warps x 8 heads");
 static_assert(kScratchBytes >= 4 * 16 * (128 + 2) * 4, "combine buffers, 4 warps x 16 heads");
-static_assert(kScratchBytes >= kHeadsPerRange * 128 * 4, "group-summed queries");
+static_assert(kScratchBytes >= kHeadsPerRange * 128 * 4, "group-summed queries, shared");
+static_assert(kScratchBytes >= 8 * 8 * 128 * 4, "group-summed queries, one copy per warp");
 
 // Launch shape for a head dimension D and NT n-tiles of 8 query heads (NT = 1: groups
 // of up to 8 query heads, NT = 2: up to 16).  kCW consumer warps (threads 0 .. 32 kCW - 1)
@@ -89,9 +91,17 @@ struct Ring {
   __device__ static __forceinline__ uint32_t phase(uint32_t n) { return (n / kPer) & 1u; }
 };
 
+// Score items of up to 8 heads and groups of up to 8 query heads (NT = 1) get their raw q
+// rows staged by a bulk copy into one of two slots, so that no consumer waits on a global
+// load of q (a dependent load costs microseconds while HBM is saturated).
+constexpr int kQSlotBytes = 8 * 8 * 128 * 2;
+template <int NT>
+constexpr int q_stage_bytes() { return NT == 1 ? 2 * kQSlotBytes : 0; }
+
 template <int D, int NT>
 constexpr size_t fused_smem_bytes() {
-  return 1024 + Ring<D, NT>::kBytes + kScratchBytes;   // 1024: alignment of the ring base
+  // 1024: alignment of the ring base
+  return 1024 + Ring<D, NT>::kBytes + kScratchBytes + q_stage_bytes<NT>();
 }
 
 enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4 };
@@ -100,7 +110,7 @@ enum : int { kAttnEveryBlock = 1, kAttnAppendLast = 2 };
 // A work item as the producer hands it to the consumers.
 struct Desc {
   int kind;
-  int first;   // unused (kept 0)
+  int first;   // score: staged q slot (0 / 1), or -1 when q is read from global memory
   int count;   // stages of the item (attention: pages)
   int row;     // score / select: sequence b; attention / empty row: b * H + h
   int x0;      // score / select: first head h0; attention: split
@@ -114,9 +124,12 @@ struct FusedShared {
   uint64_t empty[kMaxStages];   // stage consumed (one consumer warp)
   uint64_t dfull[kDescs];       // descriptor written
   uint64_t dempty[kDescs];      // descriptor read by every consumer warp
+  uint64_t qfull[2];            // staged q rows landed
+  uint64_t qempty[2];           // staged q rows read by every consumer warp
   int4 meta[kMaxStages];        // attention: {page, ntok}; score: {j of first page, pages, valid mask}
   Desc desc[kDescs];
   int plist[kProducers][kMaxScoreChunk];  // producers: pages of the current score item
+  int score_arrive[16];         // consumers: warps done with a score item (kScoreSlots)
   int flag;                     // consumers: last-arriver flag of the split merge
   int abort;                    // set after a wait of this CTA timed out
 };
@@ -160,7 +173,7 @@ __device__ __forceinline__ bool wait_flag(const int32_t *flag, int target, Fused
 // Optional cycle counters per (CTA, warp) for tuning (compile with -DKIN_TRACE_CYCLES;
 // off in the library build).  Lane 0 of each warp accumulates clock64() deltas into slots.
 #ifdef KIN_TRACE_CYCLES
-constexpr int kTraceCtas = 160, kTraceWarps = 12, kTraceSlots = 16;
+constexpr int kTraceCtas = 160, kTraceWarps = 12, kTraceSlots = 20;
 __device__ unsigned long long g_trace[kTraceCtas * kTraceWarps * kTraceSlots];
 // Per-thread accumulators (registers / local memory), flushed once per warp at exit.
 struct TraceAcc {
@@ -194,13 +207,13 @@ enum { kTrTotal = 0, kTrPWaitEmpty = 1, kTrPIssue = 2, kTrPMeta = 3, kTrPReady =
 enum { kTrCWaitFull = 1, kTrCPage = 2, kTrCDesc = 3, kTrCEpilogue = 4, kTrCScore = 5,
        kTrCSelect = 6, kTrCPages = 7, kTrCItems = 8, kTrCQ = 9, kTrCScoreQ = 10,
        kTrCScoreWait = 11, kTrCEpiBar = 12, kTrCSelWait = 13, kTrCScoreComp = 14,
-       kTrCSelComp = 15 };
+       kTrCSelComp = 15, kTrCSelKeys = 16, kTrCSelPass = 17 };
 
 __device__ __forceinline__ uint32_t score_key(float s) {
-  if (s != s) return 0u;             // NaN ranks below every number
-  s = s + 0.0f;                      // -0 and +0 compare equal
-  const uint32_t u = __float_as_uint(s);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  // order-preserving 32-bit key: -0 and +0 equal, NaN below every number (branch-free)
+  const uint32_t u = __float_as_uint(s + 0.0f);
+  const uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return s != s ? 0u : k;
 }
 
 // Kept blocks of one row, by one warp: {nb-1} plus the m largest of the n scores
@@ -283,82 +296,85 @@ __device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *k
   if (lane == 0) out[m] = nb - 1;
 }
 
-// The same selection with the row's keys held in registers: lane l holds the keys of
-// candidates j = l + 32 i, i < KPL (n <= 32 * KPL).  Every loop is unrolled, so the
-// passes run without shared-memory reloads of the keys.
+// The same selection with the row's keys in registers (lane l holds candidates
+// j = l + 32 i, i < KPL; n <= 32 KPL) and no shared memory: the m-th largest key T is
+// built bit by bit from the highest bit where the keys differ, a bit staying set when at
+// least m keys are >= the candidate (independent compares per lane, one warp sum); then
+// every key > T is kept, and the first m - count(key > T) keys equal to T in index order.
+// Padding slots hold key 0 and real keys are at least 1 (NaN maps to 1), so no per-key
+// step needs a validity test.
 template <int KPL>
-__device__ void warp_select_reg(const float *srow, int n, int m, int nb, int *hist, int32_t *out,
-                                int lane) {
+__device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_t *out,
+                                 int lane KIN_TRACE_PARAM) {
+  KIN_TIC(t_k);
   uint32_t key[KPL];
+  const int nv = n > lane ? (n - lane + 31) / 32 : 0;   // this lane's candidates
+  {
+    float sv[KPL];   // every load issued before any is used
 #pragma unroll
-  for (int i = 0; i < KPL; ++i) {
-    const int j = lane + 32 * i;
-    key[i] = j < n ? score_key(__ldcg(srow + j)) : 0u;
+    for (int i = 0; i < KPL; ++i) sv[i] = i < nv ? __ldcg(srow + lane + 32 * i) : 0.f;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 1u) : 0u;
   }
+  KIN_TOC(kTrCSelKeys, t_k);
   if (m > 0) {
-    uint32_t prefix = 0u, mask = 0u;
-    int remaining = m;
-#pragma unroll 1
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int i = lane; i < 256; i += 32) hist[i] = 0;
-      __syncwarp();
+    KIN_TIC(t_p);
+    uint32_t all_and = 0xffffffffu, all_or = 0u;
 #pragma unroll
-      for (int i = 0; i < KPL; ++i) {
-        if (lane + 32 * i < n && (key[i] & mask) == prefix)
-          atomicAdd(&hist[(key[i] >> shift) & 255u], 1);
-      }
-      __syncwarp();
-      int c[8], tot = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        c[i] = hist[lane * 8 + i];
-        tot += c[i];
-      }
-      int incl = tot;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_down_sync(0xffffffffu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      const int above_lane = incl - tot;
-      const bool mine = above_lane < remaining && remaining <= incl;
-      int digit = 0, above = 0;
-      if (mine) {
-        int run = above_lane;
-        for (int i = 7; i >= 0; --i) {
-          if (run + c[i] >= remaining) {
-            digit = lane * 8 + i;
-            above = run;
-            break;
-          }
-          run += c[i];
-        }
-      }
-      const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-      digit = __shfl_sync(0xffffffffu, digit, src);
-      above = __shfl_sync(0xffffffffu, above, src);
-      remaining -= above;
-      prefix |= static_cast<uint32_t>(digit) << shift;
-      mask |= 255u << shift;
-      __syncwarp();
+    for (int i = 0; i < KPL; ++i) {
+      all_and &= key[i] != 0u ? key[i] : 0xffffffffu;
+      all_or |= key[i];
     }
-    const uint32_t thr = prefix;
-    const int take_eq = remaining;
+    all_and = __reduce_and_sync(0xffffffffu, all_and);
+    all_or = __reduce_or_sync(0xffffffffu, all_or);
+    const uint32_t diff = all_and ^ all_or;
+    const int top = diff == 0u ? 0 : 32 - __clz(diff);   // bits [0, top) undecided
+    uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
+#pragma unroll 1
+    for (int b = top - 1; b >= 0; --b) {
+      const uint32_t cand = t | (1u << b);
+      int c0 = 0, c1 = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; i += 2) {
+        c0 += key[i] >= cand ? 1 : 0;
+        c1 += key[i + 1] >= cand ? 1 : 0;
+      }
+      if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1))) >= m)
+        t = cand;
+    }
+    int g0 = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) g0 += key[i] > t ? 1 : 0;
+    const int take_eq = m - static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g0)));
+    KIN_TOC(kTrCSelPass, t_p);
+    // index-order compaction: the votes first, then one running offset
     const unsigned lt = (1u << lane) - 1u;
+    unsigned keepm[KPL], eqm[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      keepm[i] = __ballot_sync(0xffffffffu, key[i] > t);
+      eqm[i] = __ballot_sync(0xffffffffu, key[i] == t);
+    }
     int written = 0, eq_seen = 0;
 #pragma unroll
     for (int i = 0; i < KPL; ++i) {
-      const bool in = lane + 32 * i < n;
-      const bool gt = in && key[i] > thr;
-      const bool eq = in && key[i] == thr;
-      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-      const bool keep = gt || (eq && eq_seen + __popc(eqm & lt) < take_eq);
-      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      unsigned km = keepm[i];
+      const int eq_here = __popc(eqm[i]);
+      int eq_take = take_eq - eq_seen;                    // equal keys still to take
+      if (eq_take >= eq_here) {
+        km |= eqm[i];
+      } else if (eq_take > 0) {                           // the first eq_take of this row
+        unsigned msk = eqm[i];
+        for (; eq_take > 0; --eq_take) {
+          const unsigned low = msk & (0u - msk);
+          km |= low;
+          msk ^= low;
+        }
+      }
       const int pos = written + __popc(km & lt);
-      if (keep && pos < m) out[pos] = lane + 32 * i;
+      if (((km >> lane) & 1u) && pos < m) out[pos] = lane + 32 * i;
       written += __popc(km);
-      eq_seen += __popc(eqm);
+      eq_seen += eq_here;
     }
   }
   if (lane == 0) out[m] = nb - 1;
@@ -427,7 +443,7 @@ __device__ bool make_desc(const FusedParams &p, int item, Desc &d) {
 
 template <int D, int NT>
 __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CUtensorMap *vmap,
-                         uint8_t *ring, FusedShared &sh) {
+                         uint8_t *ring, uint8_t *qstage, FusedShared &sh) {
   KIN_TRACE_DECL
   using R = Ring<D, NT>;
   using C = Cfg<D, NT>;
@@ -438,6 +454,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
   const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
   uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
   uint32_t nd = 0;            // descriptors read (and, by the leader, pushed)
+  uint32_t nq = 0;            // leader: score items whose q rows it staged
   int next = 0;
   if (leader && lane == 0) next = atomicAdd(p.work_next, 1);
 
@@ -473,6 +490,22 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
         if (make_desc<D>(p, item, d)) break;
       }
       KIN_TOC(kTrPNext, t_next);
+      if (d.kind == kDescScore) {
+        d.first = -1;
+        if (NT == 1 && d.x2 <= 8) {   // q rows [b, h0 G .. (h0 + hs) G) are contiguous
+          const int qslot = static_cast<int>(nq & 1u);
+          d.first = qslot;
+          if (lane == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(d.x2) * p.group * D * 2;
+            wait_bar(&sh.qempty[qslot], ((nq >> 1) & 1u) ^ 1u, sh, p.err);
+            mbar_arrive_expect_tx(&sh.qfull[qslot], bytes);
+            bulk_load(qstage + qslot * kQSlotBytes,
+                      p.q + (static_cast<int64_t>(d.row) * H * p.group + d.x0 * p.group) * D, bytes,
+                      &sh.qfull[qslot], policy);
+          }
+          ++nq;
+        }
+      }
       if (lane == 0) {
         const int slot = nd % kDescs;
         KIN_TIC(t0);
@@ -496,13 +529,24 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       int *plist = sh.plist[q];
       const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks + j0;
       KIN_TIC(t_meta);
-      for (int i = lane; i < npg; i += 32) {
-        int pg = __ldg(trow + i);
-        if (pg < 0 || pg >= p.num_pages) {
-          if (q == 0) flag_error(p.err, KIN_DEVERR_PAGE_ID);
-          pg = -1;
+      // All loads issued before any is used: one memory latency, not one per 32 pages.
+      int pgs[kMaxScoreChunk / 32];
+#pragma unroll
+      for (int k = 0; k < kMaxScoreChunk / 32; ++k) {
+        const int i = lane + 32 * k;
+        pgs[k] = i < npg ? __ldg(trow + i) : -1;
+      }
+#pragma unroll
+      for (int k = 0; k < kMaxScoreChunk / 32; ++k) {
+        const int i = lane + 32 * k;
+        if (i < npg) {
+          int pg = pgs[k];
+          if (pg < 0 || pg >= p.num_pages) {
+            if (q == 0) flag_error(p.err, KIN_DEVERR_PAGE_ID);
+            pg = -1;
+          }
+          plist[i] = pg;
         }
-        plist[i] = pg;
       }
       __syncwarp();
       KIN_TOC(kTrPMeta, t_meta);
@@ -611,39 +655,114 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
 // pipeline's pages (score stages) j = 0, 1, ... of an item it takes those with
 // j % kPPC == c, and finds them at its own sub-ring position n.
 // ----------------------------------------------------------------------------------
+// Score of the centroids of one ring stage ([pages][hs heads][d], at most 32 centroids):
+// lane l owns dimensions [l * kPer, l * kPer + kPer) of every centroid (conflict-free
+// shared reads; qs holds the group-summed queries, qs[h * D + dim]); a butterfly over the
+// 32 partial sums then leaves centroid c's score in lane c.  Loads are unconditional
+// (stale shared memory is harmless), so the unrolled loop issues them back to back;
+// invalid centroids are masked after the products.
+template <int D>
+__device__ __forceinline__ float stage_scores(const uint8_t *stage, const float *qs, int hs, int nc,
+                                              uint32_t vmask, int lane) {
+  constexpr int kPer = D / 32;
+  stage += lane * kPer * 2;
+  qs += lane * kPer;
+  float v[32];
+  int hh = 0, pi = 0;
+#pragma unroll
+  for (int cc = 0; cc < 32; ++cc) {
+    float f[kPer], qv[kPer];
+    if constexpr (kPer == 4) {
+      const uint2 raw = *reinterpret_cast<const uint2 *>(stage + cc * (D * 2));
+      f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
+      const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * D);
+      qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+    } else {
+      const uint32_t raw = *reinterpret_cast<const uint32_t *>(stage + cc * (D * 2));
+      f[0] = bf16_lo(raw); f[1] = bf16_hi(raw);
+      const float2 q2 = *reinterpret_cast<const float2 *>(qs + hh * D);
+      qv[0] = q2.x; qv[1] = q2.y;
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc = fmaf(qv[i], f[i], acc);
+    v[cc] = (cc < nc && ((vmask >> pi) & 1u)) ? acc : 0.f;
+    if (++hh == hs) {
+      hh = 0;
+      ++pi;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = upper ? v[k] : v[k + o];
+      const float keep = upper ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
 template <int D, int NT>
 __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring, float *qsum,
-                              FusedShared &sh, uint32_t &n KIN_TRACE_PARAM) {
+                              const uint8_t *qstage, FusedShared &sh, uint32_t &n, uint32_t &nqs,
+                              uint32_t &nsc KIN_TRACE_PARAM) {
   using R = Ring<D, NT>;
   using C = Cfg<D, NT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int q = warp % kProducers, c = warp / kProducers;
   const int H = p.num_kv_heads, G = p.group;
   const int b = d.row, h0 = d.x0, hs = d.x2;
-  // Group-summed queries of the range's heads: fp32, summed over g in order.  One thread
-  // per 8 consecutive dimensions of one head (16-byte loads).
+  // Group-summed queries of the range's heads (fp32, summed over g in order).  With up to
+  // 8 heads each warp builds its own copy in its slice of the scratch and needs no CTA
+  // barrier; with more, the consumer warps build one shared copy.
+  const bool private_q = hs <= 8;
+  float *qs = private_q ? qsum + warp * 8 * D : qsum;
   KIN_TIC(t_q);
-  for (int x = tid; x < hs * (D / 8); x += C::kCThreads) {
-    const int hh = x / (D / 8), c8 = (x % (D / 8)) * 8;
-    const __nv_bfloat16 *qp = p.q + (static_cast<int64_t>(b) * H * G + (h0 + hh) * G) * D + c8;
-    float acc[8], f[8];
-    Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp)), acc);
-    for (int g = 1; g < G; ++g) {
-      Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp + g * D)), f);
+  if (d.first >= 0) {
+    // q rows staged in shared memory: each warp sums its own copy, then frees the slot.
+    const int qslot = d.first;
+    const bool ok = wait_bar(&sh.qfull[qslot], (nqs >> 1) & 1u, sh, p.err);
+    ++nqs;
+    const __nv_bfloat16 *qraw = reinterpret_cast<const __nv_bfloat16 *>(qstage + qslot * kQSlotBytes);
+    for (int x = lane; x < hs * (D / 8); x += 32) {
+      const int hh = x / (D / 8), c8 = (x % (D / 8)) * 8;
+      float acc[8], f[8];
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(qraw + (hh * G) * D + c8), acc);
+      for (int g = 1; g < G; ++g) {
+        Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(qraw + (hh * G + g) * D + c8), f);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] += f[i];
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+      float4 *dst = reinterpret_cast<float4 *>(qs + hh * D + c8);
+      dst[0] = ok ? make_float4(acc[0], acc[1], acc[2], acc[3]) : make_float4(0.f, 0.f, 0.f, 0.f);
+      dst[1] = ok ? make_float4(acc[4], acc[5], acc[6], acc[7]) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    float4 *dst = reinterpret_cast<float4 *>(qsum + hh * D + c8);
-    dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.qempty[qslot]);
+  } else {
+    // q from global memory: the consumer warps build one shared copy.
+    for (int x = tid; x < hs * (D / 8); x += C::kCThreads) {
+      const int hh = x / (D / 8), c8 = (x % (D / 8)) * 8;
+      const __nv_bfloat16 *qp = p.q + (static_cast<int64_t>(b) * H * G + (h0 + hh) * G) * D + c8;
+      float acc[8], f[8];
+      Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp)), acc);
+      for (int g = 1; g < G; ++g) {
+        Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4 *>(qp + g * D)), f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += f[i];
+      }
+      float4 *dst = reinterpret_cast<float4 *>(qsum + hh * D + c8);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    C::Bar::sync();
+    qs = qsum;
   }
-  C::Bar::sync();
   KIN_TOC(kTrCScoreQ, t_q);
-  // A stage holds at most 32 centroids ([pages][heads][d]).  Lane l owns dimensions
-  // [l * kPer, l * kPer + kPer) of every centroid (conflict-free shared reads); the 32
-  // partial sums are then reduced across lanes by a butterfly that leaves centroid c's
-  // score in lane c.
-  constexpr int kPer = D / 32;
+  // The warp's stages of the item: the j-th stage of pipeline q, for j % kPPC == c.
   for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
     if (j % C::kPPC != c) continue;
     const int s = R::slot(warp, n);
@@ -655,58 +774,33 @@ __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring
     const int4 meta = sh.meta[s];
     const int jst = meta.x, np = meta.y;
     const uint32_t vmask = static_cast<uint32_t>(meta.z);
-    const uint8_t *stage = ring + s * R::kStageBytes + lane * kPer * 2;
-    const float *qs = qsum + lane * kPer;
     const int nc = ok ? np * hs : 0;
-    // Every load is unconditional (stale shared memory is harmless) so that the unrolled
-    // loop issues them back to back; invalid centroids are masked after the products.
-    float v[32];
-    int hh = 0, pi = 0;
-#pragma unroll
-    for (int cc = 0; cc < 32; ++cc) {
-      float f[kPer], qv[kPer];
-      if constexpr (kPer == 4) {
-        const uint2 raw = *reinterpret_cast<const uint2 *>(stage + cc * (D * 2));
-        f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
-        const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * D);
-        qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
-      } else {
-        const uint32_t raw = *reinterpret_cast<const uint32_t *>(stage + cc * (D * 2));
-        f[0] = bf16_lo(raw); f[1] = bf16_hi(raw);
-        const float2 q2 = *reinterpret_cast<const float2 *>(qs + hh * D);
-        qv[0] = q2.x; qv[1] = q2.y;
-      }
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < kPer; ++i) acc = fmaf(qv[i], f[i], acc);
-      v[cc] = (cc < nc && ((vmask >> pi) & 1u)) ? acc : 0.f;
-      if (++hh == hs) {
-        hh = 0;
-        ++pi;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-      const bool upper = (lane & o) != 0;
-#pragma unroll
-      for (int k = 0; k < o; ++k) {
-        const float send = upper ? v[k] : v[k + o];
-        const float keep = upper ? v[k + o] : v[k];
-        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-      }
-    }
+    const float score = stage_scores<D>(ring + s * R::kStageBytes, qs, hs, nc, vmask, lane);
     if (lane < nc) {
       const int pl = lane / hs, hl = lane % hs;
       __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
-             ((vmask >> pl) & 1u) ? v[0] : -INFINITY);
+             ((vmask >> pl) & 1u) ? score : -INFINITY);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
     KIN_TOC(kTrCScoreComp, t_sc);
   }
-  // Publish the item: the barrier orders every warp's score stores before the release.
-  C::Bar::sync();
-  if (tid == 0) red_add_release_gpu(p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range, 1);
+  // Publish the item: every consumer warp counts itself in at CTA scope (release /
+  // acquire), and the last one publishes all warps' scores at GPU scope (its fence is
+  // cumulative), so one warp per item pays the fence and none waits for the others.
+  // Counters are reused every kScoreSlots score items; the descriptor ring keeps the
+  // warps of a CTA fewer than kDescs items apart, so a counter is back to zero first.
+  __syncwarp();
+  if (lane == 0) {
+    int32_t *cnt = &sh.score_arrive[nsc % kScoreSlots];
+    if (atom_add_acq_rel_cta_shared(cnt, 1) == C::kCW - 1) {
+      *cnt = 0;
+      fence_acq_rel_gpu();
+      red_add_relaxed_gpu(p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range, 1);
+    }
+  }
+  ++nsc;
+  if (d.first < 0) C::Bar::sync();   // the shared group-summed queries are reused next item
 }
 
 template <int D, int NT>
@@ -719,24 +813,28 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
   const int nb = n + 1;
   KIN_TIC(t_sw);
   if (tid == 0) {
-    // Wait until every score item of this (sequence, head range) has published.
+    // Wait until every score item (chunk) of this (sequence, head range) has published.
     const int32_t *cnt = p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range;
-    wait_flag(cnt, (n + p.score_chunk - 1) / p.score_chunk, sh, p.err);
+    const int expected = (n + p.score_chunk - 1) / p.score_chunk;
+    wait_flag(cnt, expected, sh, p.err);
   }
   C::Bar::sync();
   KIN_TOC(kTrCSelWait, t_sw);
-  int *hist = reinterpret_cast<int *>(scratch) + warp * 256;
+  int *hist = reinterpret_cast<int *>(scratch) + warp * 256;   // longer rows only
   KIN_TIC(t_sel);
   for (int hh = warp; hh < hs; hh += C::kCW) {
     const int row = b * H + h0 + hh;
     const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
     int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
+    const int m = p.top_k - 1;
     if (n <= 32 * 16)
-      warp_select_reg<16>(srow, n, p.top_k - 1, nb, hist, out, lane);
+      warp_select_bits<16>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
+    else if (n <= 32 * 32)
+      warp_select_bits<32>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
     else if (n <= 32 * 64)
-      warp_select_reg<64>(srow, n, p.top_k - 1, nb, hist, out, lane);
+      warp_select_bits<64>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
     else
-      warp_select(srow, n, p.top_k - 1, nb, nullptr, hist, out, lane);
+      warp_select(srow, n, m, nb, nullptr, hist, out, lane);
     __syncwarp();
     if (lane == 0) st_release_gpu(p.ready + row, 1);
     __syncwarp();
@@ -841,10 +939,13 @@ __device__ void consume_attention(const FusedParams &p, const Desc &d, uint8_t *
 }
 
 template <int D, int NT>
-__device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch, FusedShared &sh) {
+__device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
+                         const uint8_t *qstage, FusedShared &sh) {
   using C = Cfg<D, NT>;
   KIN_TRACE_DECL
   uint32_t n = 0;   // this warp's own pages / score stages so far (its sub-ring position)
+  uint32_t nqs = 0;  // score items with staged q rows so far
+  uint32_t nsc = 0;  // score items so far
   const int tid = threadIdx.x, lane = tid & 31;
   uint32_t nd = 0;
   KIN_TIC(t_start);
@@ -863,7 +964,7 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch, 
     KIN_COUNT(kTrCItems, 1);
     if (d.kind == kDescScore) {
       KIN_TIC(t0);
-      consume_score<D, NT>(p, d, ring, reinterpret_cast<float *>(scratch), sh, n KIN_TRACE_ARG);
+      consume_score<D, NT>(p, d, ring, reinterpret_cast<float *>(scratch), qstage, sh, n, nqs, nsc KIN_TRACE_ARG);
       KIN_TOC(kTrCScore, t0);
     } else if (d.kind == kDescSelect) {
       KIN_TIC(t0);
@@ -896,6 +997,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::kAllThreads, 1)
   __shared__ FusedShared sh;
   uint8_t *ring = align1024(smem_raw);
   uint8_t *scratch = ring + Ring<D, NT>::kBytes;
+  uint8_t *qstage = scratch + kScratchBytes;   // q_stage_bytes<NT>(), 16-byte aligned
   const int tid = threadIdx.x;
   if (tid == 0) {
     for (int s = 0; s < Ring<D, NT>::kStages; ++s) {
@@ -906,14 +1008,19 @@ __global__ void __launch_bounds__(Cfg<D, NT>::kAllThreads, 1)
       mbar_init(&sh.dfull[i], 1);
       mbar_init(&sh.dempty[i], C::kCW + kProducers);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.qfull[i], 1);
+      mbar_init(&sh.qempty[i], C::kCW);
+    }
+    for (int i = 0; i < kScoreSlots; ++i) sh.score_arrive[i] = 0;
     sh.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
   if ((tid >> 5) >= C::kCW)
-    producer<D, NT>(p, &kmap, &vmap, ring, sh);
+    producer<D, NT>(p, &kmap, &vmap, ring, qstage, sh);
   else
-    consumer<D, NT>(p, ring, scratch, sh);
+    consumer<D, NT>(p, ring, scratch, qstage, sh);
 }
 
 template <int D, int NT>
@@ -949,7 +1056,7 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
 int fused_max_score_chunk() { return kMaxScoreChunk; }
 
 #ifdef KIN_TRACE_CYCLES
-// Copy out (and clear) the cycle counters: [CTA][warp][slot], 160 x 12 x 16 words.
+// Copy out (and clear) the cycle counters: [CTA][warp][slot], 160 x 12 x 20 words.
 cudaError_t trace_take(unsigned long long *host, size_t words) {
   const size_t n = sizeof(g_trace) / sizeof(g_trace[0]);
   cudaError_t e = cudaMemcpyFromSymbol(host, g_trace, (words < n ? words : n) * 8);

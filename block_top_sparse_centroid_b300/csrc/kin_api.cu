@@ -347,10 +347,13 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.n_attn_items = pl.rows * pl.max_splits;
     fp.append_final = append;
     fp.sm_scale = a->sm_scale;
+    // One launch: score, select and attention items through one work queue, so the
+    // scoring of later rows overlaps the attention of earlier ones.
     if ((s = record(events, 1, stream)) != KIN_OK) return s;
     if ((s = record(events, 2, stream)) != KIN_OK) return s;
-    cudaError_t e = launch_fused(c->head_dim, fp, &kmap, &vmap, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel launch");
+    const FusedParams f2 = fp;
+    cudaError_t e = launch_fused(c->head_dim, f2, &kmap, &vmap, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel launch (attention)");
     if ((s = record(events, 3, stream)) != KIN_OK) return s;
     return ok();
   }

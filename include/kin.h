@@ -183,13 +183,15 @@ KIN_API kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
                                                kin_stream_t stream);
 
 /* Measurement variant of kin_blocktopk_decode (mode 0) or kin_dense_decode (mode 1):
- * identical work, plus cudaEventRecord of the caller's events on `stream` around the
- * kernels: events[0] before the first kernel, events[1] after scoring, events[2] after
- * selection, events[3] after attention (dense: events[1] and [2] are recorded right
- * after events[0]).  events: host array of 4 created cudaEvent_t handles.  Used to
- * time each kernel of a step without a profiler.  While `stream` is being captured into
- * a CUDA graph the records are made with cudaEventRecordExternal, so that they become
- * event-record nodes and every replay of the graph timestamps its kernels. */
+ * identical work, plus cudaEventRecord of the caller's events on `stream`: events[0]
+ * before the step (the clearing of the workspace counters), events[3] after its last
+ * kernel.  For bf16 caches the step is one kernel and events[1] and events[2] are
+ * recorded right before it; for fp32 caches events[1] follows scoring and events[2]
+ * selection (dense: both right after events[0]).  events: host array of 4 created
+ * cudaEvent_t handles.  Used to time a step's kernels without a profiler.  While `stream`
+ * is being captured into a CUDA graph the records are made with cudaEventRecordExternal,
+ * so that they become event-record nodes and every replay of the graph timestamps its
+ * kernels. */
 KIN_API kin_status kin_decode_timed(const kin_kv_cache *cache, const kin_decode_args *args,
                                     int32_t mode, void *const *events, kin_stream_t stream);
 

@@ -216,3 +216,22 @@ def test_decode_appends_completed_final_blocks(dtype, d, dense):
     check_centroids(inp, st.cents, inp.complete_pages().tolist())
     compare_rows(inp, res, all_rows(cfg), dense=dense)
     assert st.error_bits() == 0
+
+
+def test_many_equal_scores_take_lowest_indices():
+    # every candidate block has the same keys, so every score ties: more tied candidates
+    # than a warp holds at the cut (the selection's general path), lowest indices kept
+    cfg = _cfg("ties", H=2, G=2, k=8, lens=(16 * 100 + 3, 16 * 40), seed=19)
+    inp = W.generate(cfg)
+    for b in range(cfg.batch):
+        nb = (int(inp.seq_lens[b]) + 15) // 16
+        tab = inp.block_table[b]
+        for j in range(1, nb - 1):
+            inp.k_pages[int(tab[j])] = inp.k_pages[int(tab[0])]
+    st = DeviceState(inp)
+    res = st.decode()
+    for b in range(cfg.batch):
+        nb = (int(inp.seq_lens[b]) + 15) // 16
+        for h in range(cfg.num_kv_heads):
+            assert list(res["sel"][b, h]) == list(range(cfg.top_k - 1)) + [nb - 1]
+    compare_rows(inp, res, all_rows(cfg))
