@@ -29,7 +29,10 @@ sys.path.insert(0, ROOT)
 METRIC = "block-top-k decode: seq-steps/s, achieved HBM GB/s vs peak, speedup vs dense"
 UNIT = "seq-steps/s"
 L2_FLUSH_BYTES = 256 << 20       # > 126 MB of L2
-ATTN_SOURCE = os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", "decode_fused.cu")
+# every source the fused decode kernel is compiled from (its launch plan included)
+KERNEL_SOURCES = [os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", f)
+                  for f in ("decode_fused.cu", "attn_common.cuh", "kin_common.cuh",
+                            "kin_internal.h", "kin_api.cu")]
 
 
 def parse():
@@ -89,16 +92,23 @@ def peaks():
     return 6400.0, "fallback"
 
 
-def traffic_record():
-    """DRAM bytes per attention launch from the committed ncu summary, if it is current."""
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def traffic_record(workload_name: str):
+    """DRAM bytes per fused-kernel launch from the committed ncu summary, if it was taken
+    on this workload and on the kernel sources as they are now (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p))
-    sha = hashlib.sha256(open(ATTN_SOURCE, "rb").read()).hexdigest()
-    if rec.get("source_sha256") != sha:
+    if rec.get("source_sha256") != kernel_source_sha():
         return None
-    return rec
+    return rec.get("workloads", {}).get(workload_name)
 
 
 class ClockSampler:
@@ -324,7 +334,7 @@ def main() -> int:
     attn_s = statistics.mean(sp["attn_ms"]) / 1e3
     peak, peak_kind = peaks()
     achieved = attn_bytes / attn_s / 1e9
-    trec = traffic_record()
+    trec = traffic_record(describe(cfg))
 
     e2e = None
     if not args.no_e2e:
