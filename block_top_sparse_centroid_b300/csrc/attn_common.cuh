@@ -240,9 +240,9 @@ struct WarpSoftmaxT {
       const float s3 = v1 ? (sc[nt][3] + sd[nt][3]) * scale_log2 : -INFINITY;
       float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);   // over this lane's two tokens
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {                 // over the 8 lanes of a column
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+      for (int sh = 4; sh < 32; sh <<= 1) {              // over the 8 lanes of a column
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, sh));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, sh));
       }
       const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
       const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
@@ -281,9 +281,9 @@ struct WarpSoftmaxT {
     for (int nt = 0; nt < NT; ++nt) {
       float s0 = l[nt][0], s1 = l[nt][1];
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
-        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, sh);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, sh);
       }
       const int q0 = 8 * nt + 2 * tq;
       if (gq == 0) {

@@ -117,6 +117,9 @@ struct Desc {
   int x1;      // score: first candidate j0; select: candidates n; attention: splits
   int x2;      // score / select: heads in the range; attention: kAttn* flags
   int x3;      // tokens L of the sequence
+#ifdef KIN_TRACE_CYCLES
+  int item;
+#endif
 };
 
 struct FusedShared {
@@ -131,6 +134,7 @@ struct FusedShared {
   int plist[kProducers][kMaxScoreChunk];  // producers: pages of the current score item
   int score_arrive[16];         // consumers: warps done with a score item (kScoreSlots)
   int flag;                     // consumers: last-arriver flag of the split merge
+  int sel_done;                 // consumers: select items finished (read by the queue leader)
   int abort;                    // set after a wait of this CTA timed out
 };
 
@@ -170,6 +174,19 @@ __device__ __forceinline__ bool wait_flag(const int32_t *flag, int target, Fused
   return false;
 }
 
+// Bounded wait until the shared counter *cnt >= target.  Same abort rule as wait_bar.
+__device__ __forceinline__ bool wait_shared_count(const int *cnt, int target, FusedShared &sh,
+                                                  int32_t *err) {
+  for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+    if (*reinterpret_cast<const volatile int *>(cnt) >= target) return true;
+    if ((i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0) return false;
+    __nanosleep(32);
+  }
+  *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+  flag_error(err, KIN_DEVERR_TIMEOUT);
+  return false;
+}
+
 // Optional cycle counters per (CTA, warp) for tuning (compile with -DKIN_TRACE_CYCLES;
 // off in the library build).  Lane 0 of each warp accumulates clock64() deltas into slots.
 #ifdef KIN_TRACE_CYCLES
@@ -191,7 +208,19 @@ __device__ __forceinline__ void trace_flush(const TraceAcc &t) {
 #define KIN_TIC(name) const long long name = clock64()
 #define KIN_TOC(slot, name) (tr_.v[slot] += clock64() - (name))
 #define KIN_COUNT(slot, n) (tr_.v[slot] += (n))
+// Per-item timeline: {cta, fetched, ready seen, consume begin, consume end, kind} in
+// globaltimer nanoseconds, for the first kTraceItems work items.
+constexpr int kTraceItems = 1 << 16;
+__device__ unsigned long long g_items[kTraceItems * 8];
+__device__ __forceinline__ unsigned long long gtime() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+#define KIN_ITEM_STAMP(item, field, value) \
+  do { if ((item) >= 0 && (item) < kTraceItems) g_items[(item) * 8 + (field)] = (value); } while (0)
 #else
+#define KIN_ITEM_STAMP(item, field, value) do {} while (0)
 #define KIN_TRACE_DECL
 #define KIN_TRACE_PARAM
 #define KIN_TRACE_ARG
@@ -297,10 +326,12 @@ __device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *k
 }
 
 // The same selection with the row's keys in registers (lane l holds candidates
-// j = l + 32 i, i < KPL; n <= 32 KPL) and no shared memory: the m-th largest key T is
-// built bit by bit from the highest bit where the keys differ, a bit staying set when at
-// least m keys are >= the candidate (independent compares per lane, one warp sum); then
-// every key > T is kept, and the first m - count(key > T) keys equal to T in index order.
+// j = l + 32 i, i < KPL; n <= 32 KPL) and no shared memory.  The m-th largest key T is
+// built bit by bit from the highest bit where the keys differ: a bit stays set when at
+// least m keys are >= the candidate (independent compares per lane, one warp sum).  The
+// search stops early once exactly m keys are >= the prefix built so far: those are the
+// m largest, and no key outside them equals one inside.  Otherwise (T is tied) every
+// key > T is kept, and the first m - count(key > T) keys equal to T in index order.
 // Padding slots hold key 0 and real keys are at least 1 (NaN maps to 1), so no per-key
 // step needs a validity test.
 template <int KPL>
@@ -317,6 +348,7 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_
     for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 1u) : 0u;
   }
   KIN_TOC(kTrCSelKeys, t_k);
+  const unsigned lt = (1u << lane) - 1u;
   if (m > 0) {
     KIN_TIC(t_p);
     uint32_t all_and = 0xffffffffu, all_or = 0u;
@@ -330,8 +362,9 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_
     const uint32_t diff = all_and ^ all_or;
     const int top = diff == 0u ? 0 : 32 - __clz(diff);   // bits [0, top) undecided
     uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
+    int cnt_t = n;   // keys >= t: every real key shares the bits above `top`
 #pragma unroll 1
-    for (int b = top - 1; b >= 0; --b) {
+    for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
       const uint32_t cand = t | (1u << b);
       int c0 = 0, c1 = 0;
 #pragma unroll
@@ -339,42 +372,53 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_
         c0 += key[i] >= cand ? 1 : 0;
         c1 += key[i + 1] >= cand ? 1 : 0;
       }
-      if (static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1))) >= m)
+      const int c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
+      if (c >= m) {
         t = cand;
-    }
-    int g0 = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) g0 += key[i] > t ? 1 : 0;
-    const int take_eq = m - static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g0)));
-    KIN_TOC(kTrCSelPass, t_p);
-    // index-order compaction: the votes first, then one running offset
-    const unsigned lt = (1u << lane) - 1u;
-    unsigned keepm[KPL], eqm[KPL];
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      keepm[i] = __ballot_sync(0xffffffffu, key[i] > t);
-      eqm[i] = __ballot_sync(0xffffffffu, key[i] == t);
-    }
-    int written = 0, eq_seen = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      unsigned km = keepm[i];
-      const int eq_here = __popc(eqm[i]);
-      int eq_take = take_eq - eq_seen;                    // equal keys still to take
-      if (eq_take >= eq_here) {
-        km |= eqm[i];
-      } else if (eq_take > 0) {                           // the first eq_take of this row
-        unsigned msk = eqm[i];
-        for (; eq_take > 0; --eq_take) {
-          const unsigned low = msk & (0u - msk);
-          km |= low;
-          msk ^= low;
-        }
+        cnt_t = c;
       }
-      const int pos = written + __popc(km & lt);
-      if (((km >> lane) & 1u) && pos < m) out[pos] = lane + 32 * i;
-      written += __popc(km);
-      eq_seen += eq_here;
+    }
+    KIN_TOC(kTrCSelPass, t_p);
+    if (cnt_t == m) {
+      // the keys >= t are exactly the m largest: index-order compaction of one vote each
+      unsigned km[KPL];
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) km[i] = __ballot_sync(0xffffffffu, key[i] >= t);
+      int written = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) {
+        if ((km[i] >> lane) & 1u) out[written + __popc(km[i] & lt)] = lane + 32 * i;
+        written += __popc(km[i]);
+      }
+    } else {
+      // t is the m-th largest key and is tied
+      int g0 = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) g0 += key[i] > t ? 1 : 0;
+      const int take_eq =
+          m - static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g0)));
+      int written = 0, eq_seen = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; ++i) {   // unrolled: key[] stays in registers
+        unsigned km = __ballot_sync(0xffffffffu, key[i] > t);
+        const unsigned eqm = __ballot_sync(0xffffffffu, key[i] == t);
+        const int eq_here = __popc(eqm);
+        int eq_take = take_eq - eq_seen;                    // equal keys still to take
+        if (eq_take >= eq_here) {
+          km |= eqm;
+        } else if (eq_take > 0) {                           // the first eq_take of this row
+          unsigned msk = eqm;
+          for (; eq_take > 0; --eq_take) {
+            const unsigned low = msk & (0u - msk);
+            km |= low;
+            msk ^= low;
+          }
+        }
+        const int pos = written + __popc(km & lt);
+        if (((km >> lane) & 1u) && pos < m) out[pos] = lane + 32 * i;
+        written += __popc(km);
+        eq_seen += eq_here;
+      }
     }
   }
   if (lane == 0) out[m] = nb - 1;
@@ -455,6 +499,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
   uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
   uint32_t nd = 0;            // descriptors read (and, by the leader, pushed)
   uint32_t nq = 0;            // leader: score items whose q rows it staged
+  int sel_taken = 0;          // leader: select items taken (compared with sh.sel_done)
   int next = 0;
   if (leader && lane == 0) next = atomicAdd(p.work_next, 1);
 
@@ -486,8 +531,26 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       while (true) {
         const int item = __shfl_sync(0xffffffffu, next, 0);
         if (item >= total) break;
-        if (lane == 0) next = atomicAdd(p.work_next, 1);   // prefetch the one after
-        if (make_desc<D>(p, item, d)) break;
+        const bool is_select = item >= p.n_score_items && item < p.n_score_items + p.n_select_items;
+        sel_taken += is_select ? 1 : 0;
+        if (lane == 0) {
+          // A CTA holds at most two unfinished select items: a run of selections queued
+          // behind one another in one CTA would hold back every row they release.
+          if (sel_taken >= 2) wait_shared_count(&sh.sel_done, sel_taken - 1, sh, p.err);
+          next = atomicAdd(p.work_next, 1);   // prefetch the one after
+        }
+        const bool ok = make_desc<D>(p, item, d);
+        if (is_select && !ok) --sel_taken;   // a row kept whole: no descriptor, no selection
+        if (ok) {
+#ifdef KIN_TRACE_CYCLES
+          d.item = item;
+          if (lane == 0) {
+            KIN_ITEM_STAMP(item, 0, blockIdx.x);
+            KIN_ITEM_STAMP(item, 1, gtime());
+          }
+#endif
+          break;
+        }
       }
       KIN_TOC(kTrPNext, t_next);
       if (d.kind == kDescScore) {
@@ -580,6 +643,9 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
         if (lane == 0) wait_flag(p.ready + row, 1, sh, p.err);
         __syncwarp();
         KIN_TOC(kTrPReady, t0);
+#ifdef KIN_TRACE_CYCLES
+        if (lane == 0 && q == 0) KIN_ITEM_STAMP(d.item, 2, gtime());
+#endif
       }
       const int32_t *srow = p.sel + static_cast<int64_t>(row) * p.top_k;
       const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
@@ -657,13 +723,21 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
 // ----------------------------------------------------------------------------------
 // Score of the centroids of one ring stage ([pages][hs heads][d], at most 32 centroids):
 // lane l owns dimensions [l * kPer, l * kPer + kPer) of every centroid (conflict-free
-// shared reads; qs holds the group-summed queries, qs[h * D + dim]); a butterfly over the
-// 32 partial sums then leaves centroid c's score in lane c.  Loads are unconditional
-// (stale shared memory is harmless), so the unrolled loop issues them back to back;
-// invalid centroids are masked after the products.
+// shared reads), and a butterfly over the 32 partial sums leaves centroid c's score in
+// lane c.  QS > 0: the range has QS heads and the lane's slice of the group-summed queries
+// sits in registers (qr[h][i], loaded once per item); QS = 0: any number of heads, the
+// queries are read from shared memory (qs[h * D + dim]) for each centroid.  Loads are
+// unconditional (stale shared memory is harmless), so the unrolled loop issues them back
+// to back; invalid centroids are masked after the products.
 template <int D>
-__device__ __forceinline__ float stage_scores(const uint8_t *stage, const float *qs, int hs, int nc,
-                                              uint32_t vmask, int lane) {
+struct QRegs {
+  float v[8][D / 32];
+};
+
+template <int D, int QS>
+__device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<D> &qr,
+                                              const float *qs, int hs, int nc, uint32_t vmask,
+                                              int lane) {
   constexpr int kPer = D / 32;
   stage += lane * kPer * 2;
   qs += lane * kPer;
@@ -675,21 +749,30 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const float 
     if constexpr (kPer == 4) {
       const uint2 raw = *reinterpret_cast<const uint2 *>(stage + cc * (D * 2));
       f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
-      const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * D);
-      qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
     } else {
       const uint32_t raw = *reinterpret_cast<const uint32_t *>(stage + cc * (D * 2));
       f[0] = bf16_lo(raw); f[1] = bf16_hi(raw);
+    }
+    if constexpr (QS > 0) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) qv[i] = qr.v[cc % QS][i];
+    } else if constexpr (kPer == 4) {
+      const float4 q4 = *reinterpret_cast<const float4 *>(qs + hh * D);
+      qv[0] = q4.x; qv[1] = q4.y; qv[2] = q4.z; qv[3] = q4.w;
+    } else {
       const float2 q2 = *reinterpret_cast<const float2 *>(qs + hh * D);
       qv[0] = q2.x; qv[1] = q2.y;
     }
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc = fmaf(qv[i], f[i], acc);
-    v[cc] = (cc < nc && ((vmask >> pi) & 1u)) ? acc : 0.f;
-    if (++hh == hs) {
-      hh = 0;
-      ++pi;
+    const int page = QS > 0 ? cc / QS : pi;
+    v[cc] = (cc < nc && ((vmask >> page) & 1u)) ? acc : 0.f;
+    if constexpr (QS == 0) {
+      if (++hh == hs) {
+        hh = 0;
+        ++pi;
+      }
     }
   }
 #pragma unroll
@@ -705,6 +788,49 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const float 
   return v[0];
 }
 
+// The warp's ring stages of one score item (stages t = q, q + kProducers, ... of the item,
+// those with j % kPPC == c): wait for each, score its centroids, store them, free it.
+template <int D, int NT, int QS>
+__device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d, uint8_t *ring,
+                                             const float *qs, FusedShared &sh, uint32_t &n
+                                             KIN_TRACE_PARAM) {
+  using R = Ring<D, NT>;
+  using C = Cfg<D, NT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = warp % kProducers, c = warp / kProducers;
+  const int H = p.num_kv_heads;
+  const int b = d.row, h0 = d.x0, hs = d.x2;
+  QRegs<D> qr;
+  if constexpr (QS > 0) {
+#pragma unroll
+    for (int hh = 0; hh < QS; ++hh)
+#pragma unroll
+      for (int i = 0; i < D / 32; ++i) qr.v[hh][i] = qs[hh * D + lane * (D / 32) + i];
+  }
+  for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
+    if (j % C::kPPC != c) continue;
+    const int s = R::slot(warp, n);
+    KIN_TIC(t_w);
+    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
+    ++n;
+    KIN_TOC(kTrCScoreWait, t_w);
+    KIN_TIC(t_sc);
+    const int4 meta = sh.meta[s];
+    const int jst = meta.x, np = meta.y;
+    const uint32_t vmask = static_cast<uint32_t>(meta.z);
+    const int nc = ok ? np * hs : 0;
+    const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane);
+    if (lane < nc) {
+      const int pl = lane / hs, hl = lane % hs;
+      __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
+             ((vmask >> pl) & 1u) ? score : -INFINITY);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+    KIN_TOC(kTrCScoreComp, t_sc);
+  }
+}
+
 template <int D, int NT>
 __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring, float *qsum,
                               const uint8_t *qstage, FusedShared &sh, uint32_t &n, uint32_t &nqs,
@@ -712,7 +838,6 @@ __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring
   using R = Ring<D, NT>;
   using C = Cfg<D, NT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int q = warp % kProducers, c = warp / kProducers;
   const int H = p.num_kv_heads, G = p.group;
   const int b = d.row, h0 = d.x0, hs = d.x2;
   // Group-summed queries of the range's heads (fp32, summed over g in order).  With up to
@@ -762,28 +887,14 @@ __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring
     qs = qsum;
   }
   KIN_TOC(kTrCScoreQ, t_q);
-  // The warp's stages of the item: the j-th stage of pipeline q, for j % kPPC == c.
-  for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
-    if (j % C::kPPC != c) continue;
-    const int s = R::slot(warp, n);
-    KIN_TIC(t_w);
-    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
-    ++n;
-    KIN_TOC(kTrCScoreWait, t_w);
-    KIN_TIC(t_sc);
-    const int4 meta = sh.meta[s];
-    const int jst = meta.x, np = meta.y;
-    const uint32_t vmask = static_cast<uint32_t>(meta.z);
-    const int nc = ok ? np * hs : 0;
-    const float score = stage_scores<D>(ring + s * R::kStageBytes, qs, hs, nc, vmask, lane);
-    if (lane < nc) {
-      const int pl = lane / hs, hl = lane % hs;
-      __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
-             ((vmask >> pl) & 1u) ? score : -INFINITY);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[s]);
-    KIN_TOC(kTrCScoreComp, t_sc);
+  // The warp's stages of the item, with the queries in registers for ranges of up to 8
+  // heads (the lane's slice: hs x D / 32 values).
+  switch (hs) {
+    case 8: score_stages<D, NT, 8>(p, d, ring, qs, sh, n KIN_TRACE_ARG); break;
+    case 4: score_stages<D, NT, 4>(p, d, ring, qs, sh, n KIN_TRACE_ARG); break;
+    case 2: score_stages<D, NT, 2>(p, d, ring, qs, sh, n KIN_TRACE_ARG); break;
+    case 1: score_stages<D, NT, 1>(p, d, ring, qs, sh, n KIN_TRACE_ARG); break;
+    default: score_stages<D, NT, 0>(p, d, ring, qs, sh, n KIN_TRACE_ARG); break;
   }
   // Publish the item: every consumer warp counts itself in at CTA scope (release /
   // acquire), and the last one publishes all warps' scores at GPU scope (its fence is
@@ -841,6 +952,7 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
   }
   KIN_TOC(kTrCSelComp, t_sel);
   C::Bar::sync();   // the scratch is reused by the next item
+  if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
 }
 
 template <int D, int NT>
@@ -962,6 +1074,12 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
     ++nd;
     if (d.kind == kDescEnd) break;
     KIN_COUNT(kTrCItems, 1);
+#ifdef KIN_TRACE_CYCLES
+    if (tid == 0) {
+      KIN_ITEM_STAMP(d.item, 3, gtime());
+      KIN_ITEM_STAMP(d.item, 5, d.kind);
+    }
+#endif
     if (d.kind == kDescScore) {
       KIN_TIC(t0);
       consume_score<D, NT>(p, d, ring, reinterpret_cast<float *>(scratch), qstage, sh, n, nqs, nsc KIN_TRACE_ARG);
@@ -983,6 +1101,9 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
         for (int i = tid; i < p.top_k; i += C::kCThreads) srow[i] = -1;
       }
     }
+#ifdef KIN_TRACE_CYCLES
+    if (tid == 0) KIN_ITEM_STAMP(d.item, 4, gtime());
+#endif
   }
   KIN_TOC(kTrTotal, t_start);
   KIN_TRACE_FLUSH;
@@ -1013,6 +1134,7 @@ __global__ void __launch_bounds__(Cfg<D, NT>::kAllThreads, 1)
       mbar_init(&sh.qempty[i], C::kCW);
     }
     for (int i = 0; i < kScoreSlots; ++i) sh.score_arrive[i] = 0;
+    sh.sel_done = 0;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -1063,6 +1185,16 @@ cudaError_t trace_take(unsigned long long *host, size_t words) {
   if (e != cudaSuccess) return e;
   static unsigned long long zeros[sizeof(g_trace) / sizeof(g_trace[0])];
   return cudaMemcpyToSymbol(g_trace, zeros, sizeof(zeros));
+}
+// Copy out (and clear) the per-item timeline: [item][8] words.
+cudaError_t trace_items_take(unsigned long long *host, size_t words) {
+  const size_t n = sizeof(g_items) / sizeof(g_items[0]);
+  cudaError_t e = cudaMemcpyFromSymbol(host, g_items, (words < n ? words : n) * 8);
+  if (e != cudaSuccess) return e;
+  void *addr = nullptr;
+  e = cudaGetSymbolAddress(&addr, g_items);
+  if (e != cudaSuccess) return e;
+  return cudaMemset(addr, 0, sizeof(g_items));
 }
 #endif
 
