@@ -18,11 +18,13 @@
 //                 [heads, d] run per page) into the ring with bulk copies; the consumers
 //                 form s_j = (sum_g q_g) . c_j and store it.  The last consumer barrier of
 //                 the item publishes it with an arrival count per (sequence, head range).
-//   select items  (sequence, head range).  Each consumer warp takes rows of the range in
-//                 turn: it waits for the range's score items, runs a radix select over the
-//                 row's scores (8-bit digits, per-warp shared histograms), writes the kept
+//   select items  (sequence, head range).  After the range's score items have published,
+//                 each consumer warp takes rows of the range in turn: it builds the m-th
+//                 largest score key bit by bit over the row's keys held in registers
+//                 (a radix select over L2 for rows past 2048 candidates), writes the kept
 //                 list ascending (equal scores to the lower block index, the final block
-//                 last) and releases the row's ready flag.
+//                 last) and releases the row's ready flag.  A CTA holds at most two
+//                 unfinished select items.
 //   attention     (row, split of the kept list).  The producer waits for the row's ready
 //                 flag, reads the split's kept blocks and their pages, and stages each
 //                 page's K and V (one TMA tiled copy each, 128-byte swizzle).  Producer
