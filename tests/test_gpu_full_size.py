@@ -1,0 +1,67 @@
+"""GPU parity at the four benchmark workloads' full sizes, in the launch configuration the
+benchmark times: the same seeded inputs and shapes (so the same launch plan), one block
+top-k decode call with the fused centroid append of the pages the current token completed.
+
+Rows of full-size workloads are too many for the oracle to check all of them, so:
+* every row: the kept list is valid (ascending, distinct, min(nb, k) blocks, the final
+  block last) and every output and lse is finite;
+* a seeded sample of rows (plus the first and the last row): selection, scores, outputs
+  and lse against the oracle, one row at a time, with the tolerances of the small-size
+  tests;
+* every appended centroid: bit-exact against the oracle's centroid of that page;
+* dense decode (the comparison baseline) on a few sampled rows.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from _gpu import DeviceState, check_centroids, compare_rows  # noqa: E402
+
+SAMPLED_ROWS = 12
+
+
+def _kept_lists_valid(inp, sel):
+    cfg = inp.cfg
+    k = cfg.top_k
+    lens = inp.seq_lens.numpy().astype(np.int64)
+    nb = (lens + W.BLOCK - 1) // W.BLOCK
+    for b in range(cfg.batch):
+        want = min(int(nb[b]), k)
+        rows = sel[b]                                      # [H, k]
+        kept = rows[:, :want]
+        assert np.all(rows[:, want:] == -1), f"sequence {b}: padding of the kept list"
+        assert np.all(kept[:, -1] == nb[b] - 1), f"sequence {b}: final block not last"
+        assert np.all(kept >= 0) and np.all(kept < nb[b]), f"sequence {b}: block id out of range"
+        assert np.all(np.diff(kept, axis=1) > 0), f"sequence {b}: kept list not ascending"
+
+
+@pytest.mark.parametrize("config", [1, 2, 3, 4])
+def test_full_size_workload(config):
+    cfg = W.CONFIGS[config]
+    inp = W.generate(cfg)
+    # prefill centroids only; the decode call appends the pages the current token completed
+    st = DeviceState(inp, append=False)
+    res = st.decode(append_final=True)
+    assert st.error_bits() == 0
+
+    _kept_lists_valid(inp, res["sel"])
+    assert np.isfinite(res["out"]).all()
+    assert np.isfinite(res["lse"]).all()
+
+    rows = W.sample_rows(cfg, SAMPLED_ROWS, seed=config)
+    rows = sorted(set(rows) | {(0, 0), (cfg.batch - 1, cfg.num_kv_heads - 1)})
+    stats = compare_rows(inp, res, rows)
+    assert stats["rows"] + stats["near_tie_rows"] == len(rows)
+    assert stats["rows"] >= len(rows) - 2, stats
+
+    if st.just_pages:
+        check_centroids(inp, st.cents, st.just_pages)
+
+    dense = st.decode(dense=True)
+    assert st.error_bits() == 0
+    compare_rows(inp, dense, rows[:3], dense=True)
