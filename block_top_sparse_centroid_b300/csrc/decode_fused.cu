@@ -137,6 +137,7 @@ struct FusedShared {
   int score_arrive[16];         // consumers: warps done with a score item (kScoreSlots)
   int flag;                     // consumers: last-arriver flag of the split merge
   int sel_done;                 // consumers: select items finished (read by the queue leader)
+  int last_cta;                 // this CTA finished last (clears the counters)
   int abort;                    // set after a wait of this CTA timed out
 };
 
@@ -1145,6 +1146,21 @@ __global__ void __launch_bounds__(Cfg<D, NT>::kAllThreads, 1)
     producer<D, NT>(p, &kmap, &vmap, ring, qstage, sh);
   else
     consumer<D, NT>(p, ring, scratch, qstage, sh);
+  if (p.self_clean) {
+    // Leave the counters zero for the next call.  Each CTA counts itself out after all of
+    // its threads are done with the counters (barrier, then a cumulative GPU-scope fence);
+    // the CTA that counts out last has seen every other CTA's counter updates and clears.
+    // Every wait is bounded, so every CTA gets here, after a timeout too.
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      sh.last_cta = atomicAdd(p.exit_cnt, 1) == static_cast<int>(gridDim.x) - 1;
+      __threadfence();
+    }
+    __syncthreads();
+    if (sh.last_cta)
+      for (int i = tid; i < p.n_counters; i += C::kAllThreads) p.counters[i] = 0;
+  }
 }
 
 template <int D, int NT>

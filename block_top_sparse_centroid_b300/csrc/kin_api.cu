@@ -7,6 +7,7 @@
 
 #include "kin_common.cuh"
 #include "kin_internal.h"
+#include <algorithm>
 
 namespace kin {
 namespace {
@@ -93,15 +94,21 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
   return pl;
 }
 
-// Counters cleared by every decode call: the work-queue head, score arrivals per
-// (sequence, head range), split arrivals and ready flags per row.
+// The counters of one decode call: the work-queue head, CTAs finished, score arrivals per
+// (sequence, head range), split arrivals and ready flags per row.  They sit at the start
+// of the workspace, in an area of at least kCounterWords words that no other region
+// uses, and are zero between calls: a bf16 call whose counters fit in that area leaves
+// them zero itself (the last CTA of its kernel clears them), so it needs no clearing
+// launch; any other call clears its counters before its kernels and after them.
+constexpr size_t kCounterWords = 16384;
 struct Counters {
-  size_t work_next, score_cnt, attn_cnt, ready, count;
+  size_t work_next, exit_cnt, score_cnt, attn_cnt, ready, count;
 };
 Counters counter_layout(const kin_decode_args *a, const Plan &pl) {
   Counters k{};
   k.work_next = 0;
-  k.score_cnt = 1;
+  k.exit_cnt = 1;
+  k.score_cnt = 2;
   k.attn_cnt = k.score_cnt + static_cast<size_t>(a->batch) * pl.head_ranges;
   k.ready = k.attn_cnt + pl.rows;
   k.count = k.ready + pl.rows;
@@ -119,7 +126,7 @@ Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &
   size_t off = 0;
   L.counters = off;
   L.counter_bytes = sizeof(int32_t) * counter_layout(a, pl).count;
-  off = align256(off + L.counter_bytes);
+  off = align256(off + std::max(L.counter_bytes, sizeof(int32_t) * kCounterWords));
   L.part_ml = off;
   off = align256(off + sizeof(float) * 2 * static_cast<size_t>(pl.rows) * pl.max_splits * pl.group);
   L.part_o = off;
@@ -302,10 +309,18 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   float *scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
   int32_t *sel = a->sel_blocks != nullptr ? a->sel_blocks : reinterpret_cast<int32_t *>(ws + L.sel);
   const int append = (a->flags & KIN_DECODE_APPEND_FINAL) != 0;
+  const bool self_clean = c->dtype == KIN_BF16 && ck.count <= kCounterWords;
   if ((s = record(events, 0, stream)) != KIN_OK) return s;
-  // The workspace is scratch shared with calls of other shapes: clear the counters.
-  cudaError_t me = cudaMemsetAsync(cnt, 0, L.counter_bytes, stream);
-  if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync of the workspace counters");
+  if (!self_clean) {
+    cudaError_t me = cudaMemsetAsync(cnt, 0, L.counter_bytes, stream);
+    if (me != cudaSuccess) return cuda_fail(me, "cudaMemsetAsync of the workspace counters");
+  }
+  // After the kernels of a call that does not clear its own counters.
+  auto clear_after = [&]() -> kin_status {
+    if (self_clean) return KIN_OK;
+    cudaError_t me = cudaMemsetAsync(cnt, 0, L.counter_bytes, stream);
+    return me == cudaSuccess ? KIN_OK : cuda_fail(me, "cudaMemsetAsync of the workspace counters");
+  };
 
   if (c->dtype == KIN_BF16) {
     CUtensorMap kmap, vmap;
@@ -329,6 +344,10 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.score_cnt = cnt + ck.score_cnt;
     fp.attn_cnt = cnt + ck.attn_cnt;
     fp.ready = cnt + ck.ready;
+    fp.exit_cnt = cnt + ck.exit_cnt;
+    fp.counters = cnt;
+    fp.n_counters = static_cast<int>(ck.count);
+    fp.self_clean = self_clean ? 1 : 0;
     fp.err = a->err_flag;
     fp.num_pages = c->num_pages;
     fp.batch = a->batch;
@@ -353,7 +372,8 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     if ((s = record(events, 2, stream)) != KIN_OK) return s;
     const FusedParams f2 = fp;
     cudaError_t e = launch_fused(c->head_dim, f2, &kmap, &vmap, stream);
-    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel launch (attention)");
+    if (e != cudaSuccess) return cuda_fail(e, "fused decode kernel launch");
+    if ((s = clear_after()) != KIN_OK) return s;
     if ((s = record(events, 3, stream)) != KIN_OK) return s;
     return ok();
   }
@@ -413,6 +433,7 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   ap.sm_scale = a->sm_scale;
   cudaError_t e = launch_attention_f32(c->head_dim, ap, stream);
   if (e != cudaSuccess) return cuda_fail(e, "attention kernel launch");
+  if ((s = clear_after()) != KIN_OK) return s;
   if ((s = record(events, 3, stream)) != KIN_OK) return s;
   return ok();
 }

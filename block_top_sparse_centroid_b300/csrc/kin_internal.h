@@ -78,6 +78,10 @@ struct FusedParams {
   int32_t *score_cnt;              // [B * head_ranges] finished score items
   int32_t *attn_cnt;               // [B*H] split arrivals
   int32_t *ready;                  // [B*H] selection published
+  int32_t *exit_cnt;               // CTAs finished (self_clean only)
+  int32_t *counters;               // all of the above counters, n_counters words
+  int n_counters;
+  int self_clean;                  // the last CTA to finish zeroes the counters
   int32_t *err;
   int64_t num_pages;
   int batch, num_kv_heads, group, max_blocks;

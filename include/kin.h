@@ -104,10 +104,12 @@ typedef struct {
                              -1 padded when nb < k (block top-k only)                   */
   float *scores;          /* optional [B, H, max_blocks]: group scores of blocks
                              0..nb-2 of rows with nb > k (other entries untouched)      */
-  void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned; its
-                             contents need no initialisation (each call first clears the
-                             few counters it uses, on `stream`).  Calls that may overlap
-                             on the GPU (other streams) must not share a workspace       */
+  void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned.
+                             Zero-fill it once before its first use (cudaMemset); after
+                             that only decode calls may write it: every call leaves its
+                             counter area zero again, so calls of any shapes can share it
+                             without a clearing launch.  Calls that may overlap on the GPU
+                             (other streams) must not share a workspace                  */
   size_t workspace_bytes;
   int32_t *err_flag;      /* optional device int; KIN_DEVERR_* bits are OR-ed in       */
   int32_t flags;          /* KIN_DECODE_* bits, 0 for none                             */
@@ -175,17 +177,17 @@ KIN_API kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_
  * library keeps until the process exits.  Shapes whose kin_workspace_size exceeds 16 MiB
  * return KIN_ERR_WORKSPACE.  The first call on a device looks up the array's device
  * address (with that device current); make that first call before any stream capture.
- * All calls share the one array and it keeps the previous call's contents (each call
- * clears the counters it needs first), so calls that may overlap on the GPU -- other
- * streams, other host threads -- race and must not be issued. */
+ * All calls share the one array, which starts zero-filled and keeps the previous call's
+ * contents (every call leaves its counter area zero), so calls that may overlap on the
+ * GPU -- other streams, other host threads -- race and must not be issued. */
 KIN_API kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
                                                const kin_decode_args *args,
                                                kin_stream_t stream);
 
 /* Measurement variant of kin_blocktopk_decode (mode 0) or kin_dense_decode (mode 1):
  * identical work, plus cudaEventRecord of the caller's events on `stream`: events[0]
- * before the step (the clearing of the workspace counters), events[3] after its last
- * kernel.  For bf16 caches the step is one kernel and events[1] and events[2] are
+ * before the step, events[3] after its last kernel (and, for calls that clear their
+ * counters with memsets, after the clearing).  For bf16 caches the step is one kernel and events[1] and events[2] are
  * recorded right before it; for fp32 caches events[1] follows scoring and events[2]
  * selection (dense: both right after events[0]).  events: host array of 4 created
  * cudaEvent_t handles.  Used to time a step's kernels without a profiler.  While `stream`

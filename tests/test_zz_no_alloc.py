@@ -57,7 +57,7 @@ def test_static_scratch_matches_workspace_entry_point():
     o0, l0, s0 = buffers()
     a0 = args_for(o0, l0, s0)
     assert lib.kin_workspace_size(ctypes.byref(cache), ctypes.byref(a0), 0, ctypes.byref(need)) == 0
-    ws = torch.empty(need.value, dtype=torch.uint8, device=dev)
+    ws = torch.zeros(need.value, dtype=torch.uint8, device=dev)   # zero-filled before first use
     a0 = args_for(o0, l0, s0, ws)
     assert _call(lib, lib.kin_blocktopk_decode, cache, a0) == 0
     # the static-scratch entry point, twice in a row (the second call finds the array as
