@@ -364,6 +364,20 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.n_score_items = mode == 0 ? a->batch * pl.head_ranges * pl.chunks_per_seq : 0;
     fp.n_select_items = mode == 0 ? a->batch * pl.head_ranges : 0;
     fp.n_attn_items = pl.rows * pl.max_splits;
+    // Queue lags in rounds (one sequence per round).  At the start every CTA takes an item
+    // and prefetches the next, so the first two waves of the queue (2 x 148 items) start
+    // at once: a select item comes about two waves of score items after its sequence's
+    // score items, and an attention item about two waves of score and select items after
+    // its select, so that both normally find what they wait for done.
+    if (mode == 0) {
+      const int s_per = fp.n_score_items / a->batch, sel_per = fp.n_select_items / a->batch;
+      const int span = 2 * kPlanSMs;
+      fp.lag_select = s_per > 0 ? (span + s_per - 1) / s_per : 0;
+      fp.lag_attn = fp.lag_select + (span + s_per + sel_per - 1) / (s_per + sel_per);
+    } else {
+      fp.lag_select = fp.lag_attn = 0;
+    }
+
     fp.append_final = append;
     fp.sm_scale = a->sm_scale;
     // One launch: score, select and attention items through one work queue, so the

@@ -138,6 +138,21 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// L2 prefetches of the same boxes (no shared memory, no completion): issued ahead of the
+// copies into the ring, they keep more bytes in flight than the ring can hold.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int32_t x, int32_t y,
+                                                int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Untiled bulk copy global -> shared of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned), completion counted on an mbarrier.
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes,

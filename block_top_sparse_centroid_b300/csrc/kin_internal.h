@@ -90,6 +90,10 @@ struct FusedParams {
   int score_chunk, chunks_per_seq;   // candidate blocks per score item, items per range
   int items_per_split, splits_per_row;
   int n_score_items, n_select_items, n_attn_items;
+  // Queue order: round r holds the score items of sequence r, the select items of
+  // sequence r - lag_select and the attention items of sequence r - lag_attn (each part
+  // only when that sequence exists), so that streaming scores and attention overlap.
+  int lag_select, lag_attn;
   int append_final;
   float sm_scale;
 };
