@@ -854,6 +854,76 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
   return v[0];
 }
 
+// Score of the centroids of one ring stage for ranges of exactly 8 heads: four lanes per
+// centroid.  Lane l serves head l / 4 of every page of the stage and dimensions
+// [(l % 4) D / 4, (l % 4 + 1) D / 4) of it, so its slice of the group-summed query (D / 4
+// values, qv) stays in registers for the whole item; a page is 4 x 16-byte reads, D / 4
+// products and a two-step shuffle sum per lane.  The lane reads its 16-byte chunks in a
+// rotated order (chunk c at position (c + rot) mod D / 32) so that every 8-lane phase of a
+// read touches 8 distinct bank groups; qv is stored in the same order.  Returns nothing:
+// lanes l % 4 == 0 store the scores of head l / 4.
+template <int D>
+struct QSlice {
+  float v[D / 4];
+};
+
+template <int D>
+__device__ __forceinline__ int h8_rot(int lane) {
+  return D == 128 ? (lane >> 1) & 3 : (lane >> 2) & 1;
+}
+
+template <int D>
+__device__ __forceinline__ void load_qslice(const float *qs, int lane, QSlice<D> &qv) {
+  constexpr int kCh = D / 32;   // 16-byte chunks (8 dims) per lane
+  const int head = lane >> 2, part = lane & 3, rot = h8_rot<D>(lane);
+  const float *src = qs + head * D + part * (D / 4);
+#pragma unroll
+  for (int c = 0; c < kCh; ++c) {
+    const float *cp = src + ((c + rot) & (kCh - 1)) * 8;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) qv.v[c * 8 + k] = cp[k];
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSlice<D> &qv, int np,
+                                                uint32_t vmask, float *srow_base, int64_t sstride,
+                                                int jst, int lane) {
+  constexpr int kCh = D / 32;
+  const int head = lane >> 2, part = lane & 3, rot = h8_rot<D>(lane);
+  const uint8_t *base = stage + head * (D * 2) + part * (D / 4) * 2;
+  float acc[4];
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {   // pages of the stage (loads unconditional)
+    const uint8_t *row = base + pp * 8 * (D * 2);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCh; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(row + ((c + rot) & (kCh - 1)) * 16);
+      a0 = fmaf(qv.v[c * 8 + 0], bf16_lo(raw.x), a0);
+      a1 = fmaf(qv.v[c * 8 + 1], bf16_hi(raw.x), a1);
+      a0 = fmaf(qv.v[c * 8 + 2], bf16_lo(raw.y), a0);
+      a1 = fmaf(qv.v[c * 8 + 3], bf16_hi(raw.y), a1);
+      a0 = fmaf(qv.v[c * 8 + 4], bf16_lo(raw.z), a0);
+      a1 = fmaf(qv.v[c * 8 + 5], bf16_hi(raw.z), a1);
+      a0 = fmaf(qv.v[c * 8 + 6], bf16_lo(raw.w), a0);
+      a1 = fmaf(qv.v[c * 8 + 7], bf16_hi(raw.w), a1);
+    }
+    acc[pp] = a0 + a1;
+  }
+#pragma unroll
+  for (int pp = 0; pp < 4; ++pp) {
+    acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], 1);
+    acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], 2);
+  }
+  if (part == 0) {
+    float *dst = srow_base + head * sstride + jst;
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp)
+      if (pp < np) __stcg(dst + pp, ((vmask >> pp) & 1u) ? acc[pp] : -INFINITY);
+  }
+}
+
 // The warp's ring stages of one score item (stages t = q, q + kProducers, ... of the item,
 // those with j % kPPC == c): wait for each, score its centroids, store them, free it.
 template <int D, int NT, int QS>
@@ -867,7 +937,10 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
   const int H = p.num_kv_heads;
   const int b = d.row, h0 = d.x0, hs = d.x2;
   QRegs<D> qr;
-  if constexpr (QS > 0) {
+  QSlice<D> qv;
+  if constexpr (QS == 8) {
+    load_qslice<D>(qs, lane, qv);
+  } else if constexpr (QS > 0) {
 #pragma unroll
     for (int hh = 0; hh < QS; ++hh)
 #pragma unroll
@@ -885,11 +958,17 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
     const int jst = meta.x, np = meta.y;
     const uint32_t vmask = static_cast<uint32_t>(meta.z);
     const int nc = ok ? np * hs : 0;
-    const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane);
-    if (lane < nc) {
-      const int pl = lane / hs, hl = lane % hs;
-      __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
-             ((vmask >> pl) & 1u) ? score : -INFINITY);
+    if constexpr (QS == 8) {
+      stage_scores_h8<D>(ring + s * R::kStageBytes, qv, ok ? np : 0, vmask,
+                         p.scores + static_cast<int64_t>(b * H + h0) * p.max_blocks, p.max_blocks,
+                         jst, lane);
+    } else {
+      const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane);
+      if (lane < nc) {
+        const int pl = lane / hs, hl = lane % hs;
+        __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
+               ((vmask >> pl) & 1u) ? score : -INFINITY);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
