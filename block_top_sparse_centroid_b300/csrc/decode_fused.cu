@@ -45,12 +45,13 @@ namespace kin {
 namespace {
 
 constexpr int kProducers = 4;                       // producer warps = ring pipelines
-// L2 prefetch distance of each producer in its own attention pages: the ring holds four of
-// them per producer; the K and V tiles of the next kPrefetchPages - 4 are already on their
-// way to L2 when their copies into the ring are issued.  (Measured: dense decode 11 %
-// faster, the best-of-N workload 9 %; a like prefetch of the centroid rows of score items
-// made them slower, so score items have none.)
-constexpr int kPrefetchPages = 12;
+// L2 prefetch distance of each producer in its own attention pages.  When the producer
+// issues page l it also prefetches the K and V tiles of page l + kPrefetchPages, which then
+// stream from HBM while the producer waits for a free ring stage.  Measured over distances
+// 1..20 (distance 0 is no prefetch): 1-3 are equally best, 12 and more lose again (L2
+// pressure); at 2, dense decode is 15 % and block top-k 5-12 % faster than without.  A like
+// prefetch of the centroid rows of score items (4 stages ahead) made them slower.
+constexpr int kPrefetchPages = 2;
 constexpr int kMaxRingBytes = 160 * 1024;
 constexpr int kMaxStages = kMaxRingBytes / (64 * 64);  // stages at d = 64
 constexpr int kDescs = 8;                           // descriptor slots producer -> consumers
