@@ -38,6 +38,8 @@
 // every select item precedes every attention item, in every CTA's own sequence of work;
 // score items wait for nothing but their own copies, select items only for score items,
 // attention items only for select items.
+#include <atomic>
+
 #include "attn_common.cuh"
 #include "kin_internal.h"
 
@@ -1311,24 +1313,29 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
                      cudaStream_t stream) {
   using C = Cfg<D, NT>;
   const size_t smem = fused_smem_bytes<D, NT>();
-  static int occupancy = 0, sms = 0;
-  if (occupancy == 0) {
-    cudaError_t e = cudaFuncSetAttribute(fused_decode_kernel<D, NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  // The shared-memory attribute is per device: set it, and look up the resident CTAs, once
+  // per device (racing host threads set the same values).
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> resident[kMaxDevices];   // SMs x CTAs per SM, 0 = not yet known
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int ctas = dev >= 0 && dev < kMaxDevices ? resident[dev].load(std::memory_order_acquire) : 0;
+  if (ctas == 0) {
+    e = cudaFuncSetAttribute(fused_decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    int dev = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
+    int sms = 0, occupancy = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occupancy, fused_decode_kernel<D, NT>,
                                                       C::kAllThreads, smem);
     if (e != cudaSuccess) return e;
-    if (occupancy < 1) occupancy = 1;
+    ctas = sms * (occupancy < 1 ? 1 : occupancy);
+    if (dev >= 0 && dev < kMaxDevices) resident[dev].store(ctas, std::memory_order_release);
   }
   const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
-  const int grid = min(total, sms * occupancy);
+  const int grid = min(total, ctas);
   if (grid <= 0) return cudaSuccess;
   fused_decode_kernel<D, NT><<<grid, C::kAllThreads, smem, stream>>>(*kmap, *vmap, p);
   return cudaGetLastError();
