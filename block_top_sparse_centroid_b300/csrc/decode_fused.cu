@@ -436,6 +436,128 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_
   if (lane == 0) out[m] = nb - 1;
 }
 
+// Selection of one row by all NW consumer warps: warp w holds candidates
+// j = w 32 KPL + 32 i + lane (i < KPL), keys in registers; n <= NW 32 KPL.  The same
+// bit-by-bit search as warp_select_bits, with each pass's count summed over the warps
+// through shared memory (a per-warp partial, double-buffered by pass parity, one
+// consumer-group barrier per pass), and the same early exit.  The kept list is written in
+// index order: each warp offsets its own compaction by the counts of the warps before it.
+// xs: 64 words of shared scratch.
+template <int KPL, int NW, typename Bar>
+__device__ void cta_select_row(const float *srow, int n, int m, int nb, int32_t *out, int *xs) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int jbase = w * 32 * KPL + lane;
+  uint32_t key[KPL];
+  {
+    float sv[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) sv[i] = jbase + 32 * i < n ? __ldcg(srow + jbase + 32 * i) : 0.f;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = jbase + 32 * i < n ? max(score_key(sv[i]), 1u) : 0u;
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  int *pass_cnt = xs;           // [2][NW]
+  int *and_or = xs + 2 * NW;    // [2][NW]
+  int *wtot = xs + 4 * NW;      // [2][NW]
+  if (m > 0) {
+    uint32_t a = 0xffffffffu, o = 0u;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      a &= key[i] != 0u ? key[i] : 0xffffffffu;
+      o |= key[i];
+    }
+    a = __reduce_and_sync(0xffffffffu, a);
+    o = __reduce_or_sync(0xffffffffu, o);
+    if (lane == 0) {
+      and_or[w] = static_cast<int>(a);
+      and_or[NW + w] = static_cast<int>(o);
+    }
+    Bar::sync();
+    uint32_t all_and = 0xffffffffu, all_or = 0u;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+      all_and &= static_cast<uint32_t>(and_or[v]);
+      all_or |= static_cast<uint32_t>(and_or[NW + v]);
+    }
+    const uint32_t diff = all_and ^ all_or;
+    const int top = diff == 0u ? 0 : 32 - __clz(diff);
+    uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
+    int cnt_t = n;
+    int par = 0;
+#pragma unroll 1
+    for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
+      const uint32_t cand = t | (1u << b);
+      int c0 = 0, c1 = 0;
+#pragma unroll
+      for (int i = 0; i < KPL; i += 2) {
+        c0 += key[i] >= cand ? 1 : 0;
+        c1 += key[i + 1] >= cand ? 1 : 0;
+      }
+      const int cw = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
+      if (lane == 0) pass_cnt[par * NW + w] = cw;
+      Bar::sync();
+      int c = 0;
+#pragma unroll
+      for (int v = 0; v < NW; ++v) c += pass_cnt[par * NW + v];
+      par ^= 1;
+      if (c >= m) {
+        t = cand;
+        cnt_t = c;
+      }
+    }
+    // this warp's kept keys (and, when t is tied, its keys equal to t)
+    const bool exact = cnt_t == m;
+    int g = 0, e = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      g += exact ? (key[i] >= t ? 1 : 0) : (key[i] > t ? 1 : 0);
+      e += (!exact && key[i] == t) ? 1 : 0;
+    }
+    g = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g)));
+    e = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(e)));
+    if (lane == 0) {
+      wtot[w] = g;
+      wtot[NW + w] = e;
+    }
+    Bar::sync();
+    int g_before = 0, e_before = 0, g_all = 0;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {
+      g_all += wtot[v];
+      if (v < w) {
+        g_before += wtot[v];
+        e_before += wtot[NW + v];
+      }
+    }
+    const int take_eq = exact ? 0 : m - g_all;   // equal keys kept, lowest indices first
+    int written = g_before + min(e_before, take_eq), eq_seen = e_before;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      unsigned km = __ballot_sync(0xffffffffu, exact ? key[i] >= t : key[i] > t);
+      if (!exact) {
+        const unsigned eqm = __ballot_sync(0xffffffffu, key[i] == t);
+        const int eq_here = __popc(eqm);
+        int eq_take = take_eq - eq_seen;
+        if (eq_take >= eq_here) {
+          km |= eqm;
+        } else if (eq_take > 0) {
+          unsigned msk = eqm;
+          for (; eq_take > 0; --eq_take) {
+            const unsigned low = msk & (0u - msk);
+            km |= low;
+            msk ^= low;
+          }
+        }
+        eq_seen += eq_here;
+      }
+      const int pos = written + __popc(km & lt);
+      if (((km >> lane) & 1u) && pos < m) out[pos] = jbase + 32 * i;
+      written += __popc(km);
+    }
+  }
+  if (threadIdx.x == 0) out[m] = nb - 1;
+}
+
 // ----------------------------------------------------------------------------------
 // Producer warps.  One thread issues one page's copies every few hundred cycles (barrier
 // wait, byte-count arrival, TMA issue), so kProducers warps share the work: producer q
@@ -508,13 +630,18 @@ __device__ bool make_desc(const FusedParams &p, QueueItem qi, Desc &d) {
   }
   if (qi.kind == kItemSelect) {
     const int it = item;
-    const int b = it / p.head_ranges, hr = it % p.head_ranges;
+    const int per_seq = p.coop_select ? H : p.head_ranges;
+    const int b = it / per_seq, r = it % per_seq;
     const int L = __ldg(p.seq_lens + b);
     if (L < 1 || L > kBlock * p.max_blocks) return false;
     const int nb = (L + kBlock - 1) / kBlock;
     if (nb <= p.top_k) return false;
-    const int h0 = hr * HS;
-    d = Desc{kDescSelect, 0, 0, b, h0, nb - 1, min(HS, H - h0), L};
+    if (p.coop_select) {   // one row (head r), all consumer warps; first = 1 marks it
+      d = Desc{kDescSelect, 1, 0, b, r, nb - 1, 1, L};
+    } else {               // head range r, one warp per row
+      const int h0 = r * HS;
+      d = Desc{kDescSelect, 0, 0, b, h0, nb - 1, min(HS, H - h0), L};
+    }
     return true;
   }
   const int a = item;
@@ -1079,6 +1206,31 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
   }
   C::Bar::sync();
   KIN_TOC(kTrCSelWait, t_sw);
+  if (d.first == 1) {   // one row, all consumer warps
+    KIN_TIC(t_sel);
+    const int row = b * H + h0;
+    const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
+    int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
+    const int m = p.top_k - 1;
+    int *xs = reinterpret_cast<int *>(scratch);
+    constexpr int NW = C::kCW;
+    if (n <= NW * 32 * 2)
+      cta_select_row<2, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+    else if (n <= NW * 32 * 4)
+      cta_select_row<4, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+    else if (n <= NW * 32 * 8)
+      cta_select_row<8, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+    else if (n <= NW * 32 * 16)
+      cta_select_row<16, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+    else if (warp == 0)   // longer rows: one warp, radix select over L2
+      warp_select(srow, n, m, nb, nullptr, reinterpret_cast<int *>(scratch) + 256, out, lane);
+    C::Bar::sync();
+    if (tid == 0) st_release_gpu(p.ready + row, 1);
+    KIN_TOC(kTrCSelComp, t_sel);
+    C::Bar::sync();   // the scratch is reused by the next item
+    if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
+    return;
+  }
   int *hist = reinterpret_cast<int *>(scratch) + warp * 256;   // longer rows only
   KIN_TIC(t_sel);
   for (int hh = warp; hh < hs; hh += C::kCW) {

@@ -94,6 +94,7 @@ struct FusedParams {
   // sequence r - lag_select and the attention items of sequence r - lag_attn (each part
   // only when that sequence exists), so that streaming scores and attention overlap.
   int lag_select, lag_attn;
+  int coop_select;                 // select items are single rows, selected by all consumer warps
   int append_final;
   float sm_scale;
 };
