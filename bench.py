@@ -35,7 +35,7 @@ KERNEL_SOURCES = [os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", f
                             "kin_internal.h", "kin_api.cu")]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
@@ -47,7 +47,29 @@ def parse():
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    return ap.parse_args()
+    return ap.parse_args(argv)
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """A per-rank time reduced to the job's: its slowest rank (identity on one rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_config(cfg, rank: int):
+    """Replicas decode batches of the same shapes with their own seeds (rank 0: the
+    workload itself), so the job processes world x batch sequences per step."""
+    return cfg.scaled(seed=cfg.seed + 1000 * rank) if rank else cfg
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units all ranks processed per second of the slowest rank."""
+    return units_per_rank * world / seconds
 
 
 def workload(args):
@@ -239,8 +261,7 @@ def main() -> int:
 
     import block_top_sparse_centroid_b300 as K
     W, cfg = workload(args)
-    if rank:
-        cfg = cfg.scaled(seed=cfg.seed + 1000 * rank)   # each replica its own batch
+    cfg = replica_config(cfg, rank)
     inp = W.generate(cfg)
     B, H, Hq, d = cfg.batch, cfg.num_kv_heads, cfg.num_q_heads, cfg.head_dim
     lens = [int(x) for x in inp.seq_lens]
@@ -318,12 +339,8 @@ def main() -> int:
     if int(err.item()) != 0:
         raise RuntimeError(f"device error flag {int(err.item())}")
 
-    step_s = sum(sp["step_ms"]) / len(sp["step_ms"]) / 1e3
-    if world > 1:
-        t = torch.tensor([step_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_s = float(t.item())
-    value = B * world / step_s
+    step_s = max_over_ranks(sum(sp["step_ms"]) / len(sp["step_ms"]) / 1e3, world, dev)
+    value = whole_job_rate(B, world, step_s)
 
     byt = kv_bytes(cfg, lens)
     es = 2 if cfg.dtype == "bf16" else 4
@@ -353,12 +370,8 @@ def main() -> int:
             e1.synchronize()
             if i >= args.warmup:
                 e_ms.append(e0.elapsed_time(e1))
-        e_s = sum(e_ms) / len(e_ms) / 1e3
-        if world > 1:
-            t = torch.tensor([e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_s = float(t.item())
-        e2e = {"value": B * world / e_s, "unit": UNIT,
+        e_s = max_over_ranks(sum(e_ms) / len(e_ms) / 1e3, world, dev)
+        e2e = {"value": whole_job_rate(B, world, e_s), "unit": UNIT,
                "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
                "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
                "ms_per_step": e_s * 1e3,
@@ -395,8 +408,8 @@ def main() -> int:
         "e2e": e2e,
     }
     if de is not None:
-        dense_s = sum(de["step_ms"]) / len(de["step_ms"]) / 1e3
-        line["dense"] = {"ms_per_step": dense_s * 1e3, "seq_steps_per_s": B * world / dense_s,
+        dense_s = max_over_ranks(sum(de["step_ms"]) / len(de["step_ms"]) / 1e3, world, dev)
+        line["dense"] = {"ms_per_step": dense_s * 1e3, "seq_steps_per_s": whole_job_rate(B, world, dense_s),
                          "hbm_gbs": (byt["dense_kv"] + byt["qo"]) / dense_s / 1e9,
                          "speedup_blocktopk_over_dense": dense_s / step_s}
         line["gpu_launches"] += de["launches"]
