@@ -1,0 +1,42 @@
+"""The benchmark's roofline numerator is the oracle's byte count: bench.kv_bytes, the
+algorithmic bytes per step that the roofline divides by the kernel time, must equal the
+oracle's decode_bytes (pinned to the cost model's KV term in test_oracle_pins) term by term
+on every workload's sequence lengths, for block top-k and for dense decode."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import oracle as O  # noqa: E402
+import workloads as W  # noqa: E402
+
+
+@pytest.mark.parametrize("config", range(len(W.CONFIGS)))
+def test_roofline_bytes_are_the_oracle_byte_count(config):
+    cfg = W.CONFIGS[config]
+    lens = [int(x) for x in W._draw_lengths(cfg)]
+    es = 2 if cfg.dtype == "bf16" else 4
+    got = bench.kv_bytes(cfg, lens)
+    want = O.decode_bytes(lens, cfg.num_kv_heads, cfg.group, cfg.head_dim, cfg.top_k, es)
+    assert got["kv"] == want["kv"]
+    assert got["centroids"] == want["centroids"]
+    assert got["qo"] == want["qo"]
+    dense = O.decode_bytes(lens, cfg.num_kv_heads, cfg.group, cfg.head_dim, None, es)
+    assert got["dense_kv"] == dense["kv"]
+
+
+def test_config1_step_bytes():
+    # Qwen3-0.6B-shaped workload: 64 x 8 rows, 63 full pages + the final page of 16 tokens
+    # kept per row, 511 scored centroids per row, q and out of 64 x 16 heads; plus the 64 x 8
+    # appended centroids of the pages the current token completed (context 8192 = 512 full
+    # pages): 336,068,608 bytes, the figure the roofline uses.
+    cfg = W.CONFIGS[1]
+    byt = bench.kv_bytes(cfg, [8192] * 64)
+    append = 64 * 8 * 128 * 2
+    assert byt["kv"] == 64 * 8 * 64 * 16 * 128 * 2 * 2
+    assert byt["centroids"] == 64 * 8 * 511 * 128 * 2
+    assert byt["kv"] + byt["centroids"] + byt["qo"] + append == 336068608
