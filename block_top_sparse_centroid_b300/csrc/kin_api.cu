@@ -383,6 +383,14 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
       const int span = 2 * kPlanSMs;
       fp.lag_select = s_per > 0 ? (span + s_per - 1) / s_per : 0;
       fp.lag_attn = fp.lag_select + (span + s_per + sel_per - 1) / (s_per + sel_per);
+      if (fp.coop_select) {
+        // No more rows than CTAs: every row's selection runs on a CTA of its own anyway, so
+        // the queue takes all score items, then all select items, then all attention items
+        // (measured: 16 sequences of 8K-32K tokens 12 % faster than interleaved, 8
+        // sequences 6 %).
+        fp.lag_select = a->batch;
+        fp.lag_attn = 2 * a->batch;
+      }
     } else {
       fp.lag_select = fp.lag_attn = 0;
     }
