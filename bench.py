@@ -114,10 +114,36 @@ def peaks():
     return 6400.0, "fallback"
 
 
-def kernel_source_sha() -> str:
+def strip_comments(src: str) -> str:
+    """C/C++ source without its comments and blank space, so that only code changes (not
+    comment or layout edits) change the fingerprint of the kernel sources."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":                                   # string / char literal, kept whole
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            while i < n and src[i] != "\n":
+                i += 1
+        elif src.startswith("/*", i):
+            k = src.find("*/", i + 2)
+            i = n if k < 0 else k + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_sha(read=None) -> str:
+    """Fingerprint of the code the fused kernel is compiled from (comments excluded)."""
+    read = read or (lambda f: open(f, encoding="utf-8").read())
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(f, "rb").read())
+        h.update(strip_comments(read(f)).encode())
     return h.hexdigest()
 
 

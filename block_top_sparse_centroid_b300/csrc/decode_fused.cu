@@ -8,23 +8,26 @@
 // README, "Benchmark Block TopK Attention throughput").
 //
 // One CTA per SM: kProducers producer warps and 4 or 8 consumer warps around a ring of
-// shared-memory stages (160 KB).  HBM needs well over 100 KB in flight per SM to run near
-// its peak, and one thread issues a page's copies only every few hundred cycles, so four
-// producer warps run ahead of the consumers across work items, bounded only by the ring.
+// shared-memory stages (128 KB with 8 consumer warps, 160 KB with 4).  HBM needs well over
+// 100 KB in flight per SM to run near its peak, and one thread issues a page's copies only
+// every few hundred cycles, so four producer warps run ahead of the consumers across work
+// items, bounded only by the ring (and, for attention pages, by a short L2 prefetch).
 //
-// Work items, handed out by a global counter in this order:
-//   score items   (sequence, head range, chunk of candidate blocks).  The producer copies
+// Work items, handed out by a global counter (queue order: see queue_item):
+//   score items   (sequence, head range, chunk of candidate blocks).  The producers copy
 //                 each candidate's centroid rows for the head range (one contiguous
 //                 [heads, d] run per page) into the ring with bulk copies; the consumers
-//                 form s_j = (sum_g q_g) . c_j and store it.  The last consumer barrier of
-//                 the item publishes it with an arrival count per (sequence, head range).
-//   select items  (sequence, head range).  After the range's score items have published,
-//                 each consumer warp takes rows of the range in turn: it builds the m-th
-//                 largest score key bit by bit over the row's keys held in registers
-//                 (a radix select over L2 for rows past 2048 candidates), writes the kept
-//                 list ascending (equal scores to the lower block index, the final block
-//                 last) and releases the row's ready flag.  A CTA holds at most two
-//                 unfinished select items.
+//                 form s_j = (sum_g q_g) . c_j and store it.  The last consumer warp to
+//                 finish the item publishes it with an arrival count per (sequence, head
+//                 range).
+//   select items  (sequence, head range), one consumer warp per row; or, when there are
+//                 no more rows than CTAs, a single row selected by all consumer warps
+//                 together.  After the row's score items have published, the m-th largest
+//                 score key is built bit by bit over keys held in registers (a radix
+//                 select over L2 for rows too long for that), the kept list is written
+//                 ascending (equal scores to the lower block index, the final block last)
+//                 and the row's ready flag released.  A CTA holds at most two unfinished
+//                 select items.
 //   attention     (row, split of the kept list).  The producer waits for the row's ready
 //                 flag, reads the split's kept blocks and their pages, and stages each
 //                 page's K and V (one TMA tiled copy each, 128-byte swizzle).  Producer
@@ -33,11 +36,12 @@
 //                 fp32 accumulate) and an online softmax; the warps' states are combined
 //                 in shared memory and the row's splits merged by the last split to
 //                 arrive (attn_common.cuh).
-// Every wait is bounded (a timeout sets KIN_DEVERR_TIMEOUT) and none can deadlock: a
-// CTA takes items in queue order, so every score item precedes every select item and
-// every select item precedes every attention item, in every CTA's own sequence of work;
-// score items wait for nothing but their own copies, select items only for score items,
-// attention items only for select items.
+// Every wait is bounded (a timeout sets KIN_DEVERR_TIMEOUT) and none can deadlock: every
+// item comes after everything it waits for in the queue (score items wait for nothing but
+// their own copies, select items for their row's score items, attention items for their
+// row's selection), and a CTA takes items in queue order, so the unfinished item with the
+// smallest queue index can always progress.  The last CTA to finish zeroes the workspace
+// counters for the next call.
 #include <atomic>
 
 #include "attn_common.cuh"

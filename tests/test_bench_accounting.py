@@ -40,3 +40,18 @@ def test_config1_step_bytes():
     assert byt["kv"] == 64 * 8 * 64 * 16 * 128 * 2 * 2
     assert byt["centroids"] == 64 * 8 * 511 * 128 * 2
     assert byt["kv"] + byt["centroids"] + byt["qo"] + append == 336068608
+
+
+def test_kernel_fingerprint_ignores_comments_only():
+    # the traffic record stays valid across comment edits and goes stale on code edits
+    code = 'int f(int x) { return x + 1; }  // adds one\n/* block */ const char *s = "a//b";\n'
+    same = '// header\nint f(int x)   {\n  return x + 1;   /* body */ }\nconst char *s = "a//b";\n'
+    other = 'int f(int x) { return x + 2; }\nconst char *s = "a//b";\n'
+    strip = bench.strip_comments
+    assert strip(code) == strip(same)
+    assert strip(code) != strip(other)
+    assert '"a//b"' in strip(code)                        # string literals are kept whole
+    files = {f: code for f in bench.KERNEL_SOURCES}
+    fp = bench.kernel_source_sha(files.get)
+    assert bench.kernel_source_sha({f: same for f in bench.KERNEL_SOURCES}.get) == fp
+    assert bench.kernel_source_sha({f: other for f in bench.KERNEL_SOURCES}.get) != fp
