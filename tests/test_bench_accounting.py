@@ -15,9 +15,8 @@ import oracle as O  # noqa: E402
 import workloads as W  # noqa: E402
 
 
-@pytest.mark.parametrize("config", range(len(W.CONFIGS)))
-def test_roofline_bytes_are_the_oracle_byte_count(config):
-    cfg = W.CONFIGS[config]
+@pytest.mark.parametrize("cfg", W.CONFIGS, ids=lambda c: c.name)
+def test_roofline_bytes_are_the_oracle_byte_count(cfg):
     lens = [int(x) for x in W._draw_lengths(cfg)]
     es = 2 if cfg.dtype == "bf16" else 4
     got = bench.kv_bytes(cfg, lens)
@@ -34,7 +33,7 @@ def test_config1_step_bytes():
     # kept per row, 511 scored centroids per row, q and out of 64 x 16 heads; plus the 64 x 8
     # appended centroids of the pages the current token completed (context 8192 = 512 full
     # pages): 336,068,608 bytes, the figure the roofline uses.
-    cfg = W.CONFIGS[1]
+    cfg = W.find_config("qwen3-0.6b")
     byt = bench.kv_bytes(cfg, [8192] * 64)
     append = 64 * 8 * 128 * 2
     assert byt["kv"] == 64 * 8 * 64 * 16 * 128 * 2 * 2

@@ -40,9 +40,13 @@ def _kept_lists_valid(inp, sel):
         assert np.all(np.diff(kept, axis=1) > 0), f"sequence {b}: kept list not ascending"
 
 
-@pytest.mark.parametrize("config", [1, 2, 3, 4])
-def test_full_size_workload(config):
-    cfg = W.CONFIGS[config]
+# workload name -> seed of its sampled rows
+FULL_SIZE = {"qwen3-0.6b": 1, "qwen3-8b": 2, "qwen3-32b-ragged": 3, "best-of-n-qwen3-14b": 4}
+
+
+@pytest.mark.parametrize("name", list(FULL_SIZE))
+def test_full_size_workload(name):
+    cfg = W.find_config(name)
     inp = W.generate(cfg)
     # prefill centroids only; the decode call appends the pages the current token completed
     st = DeviceState(inp, append=False)
@@ -53,7 +57,7 @@ def test_full_size_workload(config):
     assert np.isfinite(res["out"]).all()
     assert np.isfinite(res["lse"]).all()
 
-    rows = W.sample_rows(cfg, SAMPLED_ROWS, seed=config)
+    rows = W.sample_rows(cfg, SAMPLED_ROWS, seed=FULL_SIZE[name])
     rows = sorted(set(rows) | {(0, 0), (cfg.batch - 1, cfg.num_kv_heads - 1)})
     stats = compare_rows(inp, res, rows)
     assert stats["rows"] + stats["near_tie_rows"] == len(rows)

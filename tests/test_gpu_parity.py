@@ -32,7 +32,7 @@ def _run(cfg, dense=False):
 
 
 def test_tiny_config_fp32():
-    cfg = W.CONFIGS[0]
+    cfg = W.find_config("tiny")
     inp, st, res, stats = _run(cfg)
     assert stats["rows"] == 1
     check_centroids(inp, st.cents, inp.complete_pages().tolist())
@@ -90,7 +90,7 @@ def test_topk_at_least_blocks_equals_dense():
 
 def test_unshuffled_and_shared_pages():
     # best-of-N layout: every sample shares the prompt's pages
-    cfg = W.CONFIGS[4].scaled(batch=6, ctx_lo=300, ctx_hi=900, prefix=256, steps=1)
+    cfg = W.find_config("best-of-n-qwen3-14b").scaled(batch=6, ctx_lo=300, ctx_hi=900, prefix=256, steps=1)
     inp, st, res, stats = _run(cfg)
     assert stats["rows"] + stats["near_tie_rows"] == cfg.batch * cfg.num_kv_heads
 

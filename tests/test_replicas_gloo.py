@@ -29,12 +29,13 @@ def _rank(rank: int, world: int, port: int, out) -> None:
         per_rank_s = 0.010 * (rank + 1)                    # rank 1 is the slower one
         job_s = bench.max_over_ranks(per_rank_s, world, "cpu")
         rate = bench.whole_job_rate(64, world, job_s)
-        seed = bench.replica_config(W.CONFIGS[1], rank).seed
-        shapes = bench.replica_config(W.CONFIGS[1], rank).scaled(seed=0)
+        base = W.find_config("qwen3-0.6b")
+        mine = bench.replica_config(base, rank)
+        same_shapes = mine.scaled(seed=0) == base.scaled(seed=0)
         # the reference arm: every rank but 0 returns at once, without work
         ref_rc = bench.run_reference(bench.parse(["--impl", "reference", "--steps", "1",
                                                   "--warmup", "0"])) if rank else None
-        out.put((rank, job_s, rate, seed, shapes == W.CONFIGS[1].scaled(seed=0), ref_rc))
+        out.put((rank, job_s, rate, mine.seed, same_shapes, ref_rc))
         dist.barrier()
     finally:
         dist.destroy_process_group()

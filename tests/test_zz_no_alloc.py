@@ -27,7 +27,7 @@ def test_static_scratch_matches_workspace_entry_point():
     from _gpu import DeviceState, OUT_MAX_ABS, LSE_ABS
     import block_top_sparse_centroid_b300._lib as L
     lib = L.load()
-    cfg = W.CONFIGS[1].scaled(batch=8, ctx_kind="explicit",
+    cfg = W.find_config("qwen3-0.6b").scaled(batch=8, ctx_kind="explicit",
                               lens=(8192, 8191, 4000, 17, 1600, 16 * 300, 5000, 12000), top_k=32)
     inp = W.generate(cfg)
     st = DeviceState(inp)
