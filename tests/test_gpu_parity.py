@@ -47,6 +47,17 @@ def test_group_and_head_dim(d, G):
     _run(cfg, dense=True)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("G", [1, 5])
+def test_eight_head_ranges(d, G):
+    # 8 KV heads: the score stages of a whole 8-head range (four lanes per centroid); with
+    # 19 sequences (152 rows, more than the 148 CTAs) one warp selects each row of a range
+    lens = (130, 1500, 4097, 2048, 17, 700, 16 * 33, 999, 3000, 64,
+            1201, 250, 16 * 90 + 1, 3333, 160, 2222, 801, 47, 1024)
+    cfg = _cfg(f"h8g{G}d{d}", d=d, H=8, G=G, k=8, lens=lens, seed=G * 10 + d)
+    _run(cfg)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("q_std", [None, 1.0, 4.0])
 def test_softmax_sharpness(dtype, q_std):
