@@ -58,6 +58,17 @@ def test_eight_head_ranges(d, G):
     _run(cfg)
 
 
+@pytest.mark.parametrize("H", [4, 16])
+def test_other_head_range_widths(H):
+    # 4 heads (40 rows): the queries of the range in registers, cooperative selection;
+    # 16 heads (160 rows, more than the 148 CTAs): queries read from global memory into one
+    # shared copy, two pages per score stage, two rows per selecting warp
+    lens = (130, 1500, 4097, 700, 2048, 33, 1111, 16 * 50, 2500, 401)
+    cfg = _cfg(f"h{H}", H=H, G=2, k=8, lens=lens, seed=H)
+    _run(cfg)
+    _run(cfg, dense=True)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("q_std", [None, 1.0, 4.0])
 def test_softmax_sharpness(dtype, q_std):
