@@ -72,7 +72,9 @@ typedef enum { KIN_F32 = 0, KIN_BF16 = 1 } kin_dtype;
 /* Bits OR-ed into *err_flag by the kernels. */
 #define KIN_DEVERR_PAGE_ID 1 /* a block-table or page-list entry outside [0, num_pages) */
 #define KIN_DEVERR_SEQ_LEN 2 /* a seq_len outside [1, 16 * max_blocks]                 */
-#define KIN_DEVERR_TIMEOUT 4 /* a bounded wait for an asynchronous copy gave up         */
+#define KIN_DEVERR_TIMEOUT 4 /* a bounded wait gave up: for a copy, for another CTA's
+                                result (scores published, a selection released) or for
+                                a shared counter; the kernel then winds down            */
 
 /* A paged KV cache of one attention layer (caller-owned device memory). */
 typedef struct {
