@@ -7,11 +7,13 @@ else, and it never reads anything the CUDA path computed.
 
 See ``oracle.blocktopk`` for the method and the passages each function follows.
 """
-from .blocktopk import (BLOCK, round_to_bf16, block_centroid, centroids, group_scores,
+from .blocktopk import (BLOCK, round_to_bf16, block_centroid, centroids, centroid_pair,
+                        group_scores, valid_selections,
                         select_blocks, attend, row_tokens, decode_rows, blocktopk_decode,
                         dense_decode, decode_bytes, dense_kv_bytes_per_step,
                         sparse_kv_tokens)
 
-__all__ = ["BLOCK", "round_to_bf16", "block_centroid", "centroids", "group_scores",
+__all__ = ["BLOCK", "round_to_bf16", "block_centroid", "centroids", "centroid_pair",
+           "valid_selections", "group_scores",
            "select_blocks", "attend", "row_tokens", "decode_rows", "blocktopk_decode",
            "dense_decode", "decode_bytes", "dense_kv_bytes_per_step", "sparse_kv_tokens"]

@@ -26,15 +26,22 @@ design notes of the repository):
 3. Ties in score go to the lower block index.
 4. The softmax scale sm_scale multiplies q . k inside the exponent; scoring ignores it
    (ranking is invariant to a positive scale).
-5. Precision: scores, softmax and outputs are computed in float64.  The centroid is a
-   stored code (bf16 or fp32), and a stored code is taken in the precision of the kernel
-   that produces it: keys are summed in float32 in ascending token order, scaled by
-   1/16 (exact), then rounded to the storage type (bf16: round-to-nearest-even).
+5. Precision: scores, softmax and outputs are computed in float64 from float32
+   centroids: keys are summed in float32 in ascending token order and scaled by 1/16
+   (exact).  This fp32 centroid is what selection is judged against.  The library stores a
+   bf16 cache's centroid as a pair of bf16 codes (``centroid_pair``: the fp32 mean rounded
+   to bf16, and the rounding residual rounded to bf16); ``store="bf16"`` rounds the
+   centroid to its first code, the value the library's block scores are computed from.
+6. Acceptance of another implementation's selection: it may differ from this oracle's
+   only on blocks whose oracle scores lie within 1e-3 (relative) of the last kept score;
+   ``valid_selections`` lists every kept set that rule admits.
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
 from __future__ import annotations
 
+import itertools
+import math
 from typing import Iterable, List, Optional, Sequence, Tuple
 
 import numpy as np
@@ -106,6 +113,20 @@ def centroids(k_pages: np.ndarray, page_ids: Sequence[int], store: str) -> np.nd
     return _store(mean, store)
 
 
+def centroid_pair(k_pages: np.ndarray, page_ids: Sequence[int]) -> Tuple[np.ndarray, np.ndarray]:
+    """The two bf16 codes a bf16 cache stores for each listed page's centroid.
+
+    hi = the fp32 mean rounded to bf16 (round-to-nearest-even); lo = (mean - hi) rounded
+    to bf16.  The fp32 difference is exact (hi is the rounding of the mean, so the two lie
+    within a factor of two of each other), hence hi + lo equals the fp32 mean to about 2^-16
+    of its size.  Returns (hi, lo), each [len(page_ids), H, d] float32 holding bf16 values.
+    """
+    c32 = centroids(k_pages, page_ids, "f32")
+    hi = round_to_bf16(c32)
+    lo = round_to_bf16((c32 - hi).astype(np.float32))
+    return hi, lo
+
+
 # --------------------------------------------------------------------------------------
 # Step 2: group score of each candidate block
 # --------------------------------------------------------------------------------------
@@ -144,6 +165,37 @@ def select_blocks(scores: Sequence[float], nb: int, k: int) -> List[int]:
     order = sorted(range(nb - 1), key=lambda j: (-float(scores[j]), j))
     chosen = order[: k - 1]
     return sorted(chosen + [nb - 1])
+
+
+def valid_selections(scores: Sequence[float], nb: int, k: int, rel: float = 1e-3,
+                     limit: int = 100000) -> List[List[int]]:
+    """Every kept list an implementation may return for one row under the acceptance rule.
+
+    The rule: a kept set may differ from ``select_blocks``'s only on blocks whose scores lie
+    within ``rel`` (relative) of the last kept score s_(k), i.e. where the oracle's k-th and
+    (k+1)-th scores nearly tie.  So the blocks kept outside that band are kept by every
+    admissible set, and the rest of the k-1 scored places go to any choice of blocks inside
+    the band.  Returns the sets ascending (the oracle's own among them); raises when there
+    are more than ``limit``.
+    """
+    base = select_blocks(scores, nb, k)
+    if nb <= k:
+        return [base]
+    m = k - 1
+    if m == 0:
+        return [base]
+    cand = [float(scores[j]) for j in range(nb - 1)]
+    order = sorted(range(nb - 1), key=lambda j: (-cand[j], j))
+    t = cand[order[m - 1]]
+    band = rel * abs(t)
+    near = [j for j in range(nb - 1) if abs(cand[j] - t) <= band]
+    near_set = set(near)
+    core = [j for j in base[:-1] if j not in near_set]
+    r = m - len(core)
+    n_sets = math.comb(len(near), r)
+    if n_sets > limit:
+        raise ValueError(f"{n_sets} admissible selections (limit {limit})")
+    return [sorted(core + list(c) + [nb - 1]) for c in itertools.combinations(near, r)]
 
 
 # --------------------------------------------------------------------------------------
@@ -233,8 +285,11 @@ def decode_rows(q: np.ndarray, k_pages: np.ndarray, v_pages: np.ndarray,
 
 
 def blocktopk_decode(q, k_pages, v_pages, block_table, seq_lens, sm_scale, top_k,
-                     store="bf16", rows=None) -> dict:
-    """Block top-k decode (score, select, attend) for the listed rows."""
+                     store="f32", rows=None) -> dict:
+    """Block top-k decode (score, select, attend) for the listed rows.
+
+    store="f32" (fp32 centroids) is the reference selection; store="bf16" scores with the
+    centroids rounded to bf16, the block scores a bf16 cache's first centroid code gives."""
     return decode_rows(q, k_pages, v_pages, block_table, seq_lens, sm_scale, top_k,
                        store, rows)
 

@@ -79,6 +79,69 @@ def pin_centroid_closed_forms():
             assert np.array_equal(allc[n, h], OB.block_centroid(pages[p, h], "bf16"))
 
 
+def pin_centroid_pair():
+    """The bf16 (hi, lo) code of a centroid: hi is the fp32 mean rounded to bf16, lo the
+    exact residual rounded to bf16, and hi + lo is the fp32 mean to 2^-16 of its size."""
+    # closed form: fifteen keys 1.0 and one 1 + 2^-6 (both exact in bf16) have the mean
+    # 1 + 2^-10, which bf16 (7 fraction bits) rounds to 1: hi = 1 and lo = 2^-10 exactly
+    keys = np.ones((16, 4), dtype=np.float32)
+    keys[7, :] = 1.0 + 2.0 ** -6
+    hi, lo = OB.centroid_pair(keys[None, None], [0])
+    assert np.all(hi == 1.0) and np.all(lo == 2.0 ** -10)
+    # a mean that bf16 holds exactly has no residual
+    keys = np.full((16, 4), 0.75, dtype=np.float32)
+    hi, lo = OB.centroid_pair(keys[None, None], [0])
+    assert np.all(hi == 0.75) and np.all(lo == 0.0)
+    r = _rng(12)
+    pages = (r.standard_normal((6, 2, 16, 48)) * 10.0 ** r.uniform(-3, 3, (6, 1, 1, 1))).astype(np.float32)
+    pages = _bf16_exact(pages)
+    hi, lo = OB.centroid_pair(pages, [5, 0, 3])
+    for n, p in enumerate([5, 0, 3]):
+        for h in range(2):
+            c32 = OB.block_centroid(pages[p, h], "f32")
+            assert np.array_equal(hi[n, h], _bf16_exact(c32))
+            diff64 = c32.astype(np.float64) - hi[n, h].astype(np.float64)
+            assert np.array_equal(diff64, (c32 - hi[n, h]).astype(np.float64))  # exact in fp32
+            assert np.array_equal(lo[n, h], _bf16_exact(diff64.astype(np.float32)))
+            err = np.abs(c32.astype(np.float64) - hi[n, h] - lo[n, h].astype(np.float64))
+            assert np.all(err <= 2.0 ** -16 * np.abs(c32.astype(np.float64)))
+            assert np.all(np.abs(diff64) <= 2.0 ** -8 * np.abs(hi[n, h].astype(np.float64)))
+
+
+def _admissible_by_rule(scores, nb, k, rel):
+    """Every kept set of size k that holds the final block and differs from the oracle's
+    own only on blocks whose score is within rel of the oracle's last kept score."""
+    base = OB.select_blocks(scores, nb, k)
+    if nb <= k:
+        return [base]
+    kept_scores = sorted((float(scores[j]) for j in base[:-1]), reverse=True)
+    t = kept_scores[-1] if kept_scores else None
+    out = []
+    for comb in itertools.combinations(range(nb - 1), k - 1):
+        cand = sorted(list(comb) + [nb - 1])
+        if all(abs(float(scores[j]) - t) <= rel * abs(t) for j in set(cand) ^ set(base)):
+            out.append(cand)
+    return out
+
+
+def pin_valid_selections():
+    """The admissible kept sets equal a filter of every subset by the acceptance rule."""
+    assert OB.valid_selections([5.0, 5.0, 5.0], 4, 2) == [[0, 3], [1, 3], [2, 3]]
+    assert OB.valid_selections([1.0, 9.0, 4.0], 4, 3) == [[1, 2, 3]]      # no near tie
+    assert OB.valid_selections([1.0, 9.0], 3, 5) == [[0, 1, 2]]           # nb <= k
+    r = _rng(13)
+    for trial in range(300):
+        nb = int(r.integers(2, 10))
+        k = int(r.integers(1, 6))
+        base = r.integers(1, 6, nb - 1).astype(np.float64) * 1000.0
+        jitter = r.choice([0.0, 1e-4, 5e-4, 2e-3, 1e-2], nb - 1)
+        scores = list(base * (1.0 + jitter * r.choice([-1.0, 1.0], nb - 1)))
+        got = OB.valid_selections(scores, nb, k)
+        want = _admissible_by_rule(scores, nb, k, 1e-3)
+        assert sorted(got) == sorted(want), (scores, nb, k)
+        assert OB.select_blocks(scores, nb, k) in got
+
+
 # ----------------------------------------------------------------------------- scores
 def pin_group_scores():
     r = _rng(3)
@@ -317,7 +380,8 @@ def pin_byte_accounting():
     assert byt["qo"] == 2 * len(nbs) * H * G * d * 4
 
 
-PINS = [pin_bf16_rounding, pin_centroid_closed_forms, pin_group_scores,
+PINS = [pin_bf16_rounding, pin_centroid_closed_forms, pin_centroid_pair, pin_group_scores,
+        pin_valid_selections,
         pin_selection_brute_force, pin_attention_vs_sdpa, pin_decode_against_masked_sdpa,
         pin_decode_invariants, pin_hand_worked_golden, pin_byte_accounting]
 
@@ -391,6 +455,34 @@ def _m_bf16_truncate(x):
     return (x.view(np.uint32) & np.uint32(0xFFFF0000)).view(np.float32)
 
 
+def _m_pair_no_residual(k_pages, page_ids):
+    hi, lo = _orig_pair(k_pages, page_ids)
+    return hi, np.zeros_like(lo)
+
+
+def _m_pair_residual_sign(k_pages, page_ids):
+    hi, lo = _orig_pair(k_pages, page_ids)
+    return hi, -lo
+
+
+def _m_valid_absolute_band(scores, nb, k, rel=1e-3, limit=100000):
+    # the band taken in absolute units instead of relative to the last kept score
+    base = OB.select_blocks(scores, nb, k)
+    if nb <= k or k == 1:
+        return [base]
+    cand = [float(scores[j]) for j in range(nb - 1)]
+    t = sorted(cand, reverse=True)[k - 2]
+    near = [j for j in range(nb - 1) if abs(cand[j] - t) <= rel]
+    core = [j for j in base[:-1] if j not in near]
+    return [sorted(core + list(c) + [nb - 1])
+            for c in itertools.combinations(near, k - 1 - len(core))]
+
+
+def _m_valid_only_base(scores, nb, k, rel=1e-3, limit=100000):
+    return [OB.select_blocks(scores, nb, k)]
+
+
+_orig_pair = OB.centroid_pair
 _orig_attend = OB.attend
 
 MUTANTS = {
@@ -405,6 +497,10 @@ MUTANTS = {
     "centroid_divides_by_15": ("block_centroid", _m_centroid_div15),
     "centroid_wrong_axis": ("centroids", _m_centroids_wrong_axis),
     "bf16_truncates": ("round_to_bf16", _m_bf16_truncate),
+    "pair_without_residual": ("centroid_pair", _m_pair_no_residual),
+    "pair_residual_wrong_sign": ("centroid_pair", _m_pair_residual_sign),
+    "admissible_band_absolute": ("valid_selections", _m_valid_absolute_band),
+    "admissible_only_own_set": ("valid_selections", _m_valid_only_base),
 }
 
 
