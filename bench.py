@@ -1,13 +1,18 @@
 #!/usr/bin/env python3
-"""Benchmark of block top-k decode attention (one attention layer, one decode step).
+"""Benchmark of block top-k decode attention (one attention layer).
 
-Default workload: the Qwen3-0.6B-shaped layer decode (batch 64, 16 query / 8 KV heads,
-head_dim 128, bf16, uniform context 8192, top-64 pages of 16 tokens), synthetic seeded
-inputs.  One timed step = the centroid append of the pages the current token completed
-+ one block top-k decode (score, select, sparse attention with its split merge).
+Default workload: best-of-N decode, Qwen3-14B-shaped (256 samples, 40 query / 8 KV heads,
+head_dim 128, bf16, a shared 1024-token prompt plus generated lengths U[2048, 16384],
+top-128 pages of 16 tokens), 64 consecutive decode steps, synthetic seeded inputs.  One
+timed step = one decode step of that loop: the block top-k decode (score, select, sparse
+attention with its split merge, and the centroid append of the pages the step's token
+completed).  Each step's K/V token write and seq_lens advance (the caller's part) run
+before it, outside its timed events, and are reported separately.  The Qwen3-0.6B, -8B and
+-32B-shaped single-step workloads are measured in the same run and reported under
+"configs".
 
 Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle instead (the
-reference arm): rank 0 only, a bounded sample of rows per step.
+reference arm): rank 0 only, a bounded sample of rows per step on all host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
 """
@@ -38,15 +43,18 @@ KERNEL_SOURCES = [os.path.join(ROOT, "block_top_sparse_centroid_b300", "csrc", f
 def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, help="workload index (0..4)")
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=64)
+    ap.add_argument("--config", type=int, default=4, help="workload index (0..4)")
     ap.add_argument("--batch", type=int, default=0, help="override the batch (small profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the single-step Qwen3 workloads reported under \"configs\"")
+    ap.add_argument("--other-steps", type=int, default=30)
     return ap.parse_args(argv)
 
 
@@ -199,37 +207,134 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(inp, cfg, seconds: float, rows_cap: int = 100000) -> dict:
-    """The CPU oracle as it stands, on a bounded sample of the workload's rows."""
-    import numpy as np  # noqa: F401
+
+
+# ------------------------------------------------------------------------------- oracle
+_POOL_STATE = {}
+
+
+def _bf16_to_f32(x):
+    import numpy as np
+    return (x.astype(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _pool_state(inp) -> dict:
+    """Numpy views of a workload's host inputs (no copy), for the oracle's workers."""
+    import torch
+    bf = inp.k_pages.dtype == torch.bfloat16
+    view = (lambda t: t.view(torch.int16).numpy()) if bf else (lambda t: t.numpy())
+    return dict(bf16=bf, k=view(inp.k_pages), v=view(inp.v_pages), q=view(inp.q),
+                table=inp.block_table.numpy(), lens=inp.seq_lens.numpy(), cfg=inp.cfg)
+
+
+def _oracle_row(bh) -> int:
+    """One (sequence, KV head) row of the CPU oracle, on the inputs in _POOL_STATE: the
+    row's pages gathered in block order (numpy only), then the oracle as it stands."""
+    import numpy as np
     import oracle as O
-    import workloads as W
+    st = _POOL_STATE
+    cfg = st["cfg"]
+    b, h = bh
+    G = cfg.group
+    L = int(st["lens"][b])
+    nb = (L + 15) // 16
+    pages = st["table"][b, :nb].astype(np.int64)
+    conv = _bf16_to_f32 if st["bf16"] else (lambda x: np.asarray(x, np.float32))
+    q = conv(st["q"][b:b + 1, h * G:(h + 1) * G])
+    kp = conv(st["k"][pages, h:h + 1])
+    vp = conv(st["v"][pages, h:h + 1])
+    O.blocktopk_decode(q, kp, vp, np.arange(nb, dtype=np.int64)[None, :],
+                       np.array([L], dtype=np.int64), cfg.sm_scale, cfg.top_k)
+    return 1
+
+
+def _pool_init():
+    try:
+        from threadpoolctl import threadpool_limits
+        threadpool_limits(limits=1)
+    except Exception:  # pragma: no cover
+        pass
+
+
+class OraclePool:
+    """Worker processes for timing the CPU oracle on all host cores.  They are forked
+    from this process, so create the pool before the process's first CUDA call: the
+    workers share the host inputs (copy on write, as numpy views) and use no torch."""
+
+    def __init__(self, inp, workers: int):
+        import multiprocessing as mp
+        global _POOL_STATE
+        _POOL_STATE = _pool_state(inp)
+        self.cfg = inp.cfg
+        self.workers = workers
+        self.pool = mp.get_context("fork").Pool(workers, initializer=_pool_init)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+    def rate(self, seconds: float, seed: int = 11) -> dict:
+        """Rows done in about `seconds`, cycling over a seeded sample of rows."""
+        import workloads as W
+        rows = W.sample_rows(self.cfg, 4096, seed=seed)
+        self.pool.map(_oracle_row, rows[:self.workers])        # start-up, untimed
+        nxt = 0
+        done = 0
+        t0 = time.perf_counter()
+        pending = []
+        for _ in range(2 * self.workers):
+            pending.append(self.pool.apply_async(_oracle_row, (rows[nxt % len(rows)],)))
+            nxt += 1
+        while pending:
+            pending[0].wait()
+            r = pending.pop(0)
+            done += r.get()
+            if time.perf_counter() - t0 < seconds:
+                pending.append(self.pool.apply_async(_oracle_row, (rows[nxt % len(rows)],)))
+                nxt += 1
+        return dict(rows=done, seconds=time.perf_counter() - t0)
+
+
+def oracle_rate_single(inp, seconds: float, seed: int = 11) -> dict:
+    """The same oracle rows in this process, one thread (BLAS limited to one)."""
     import contextlib
+    import workloads as W
+    global _POOL_STATE
+    _POOL_STATE = _pool_state(inp)
+    rows = W.sample_rows(inp.cfg, 4096, seed=seed)
     try:
         from threadpoolctl import threadpool_limits
         limit = threadpool_limits(limits=1)
     except Exception:  # pragma: no cover
         limit = contextlib.nullcontext()
-    rows = W.sample_rows(cfg, rows_cap, seed=11)
     done = 0
     with limit:
         t0 = time.perf_counter()
-        while True:                      # cycle over the sampled rows until the budget ends
-            for b, h in rows:
-                rp = W.row_problem(inp, b, h)
-                O.blocktopk_decode(rp["q"], rp["k_pages"], rp["v_pages"], rp["block_table"],
-                                   rp["seq_lens"], cfg.sm_scale, cfg.top_k,
-                                   store="bf16" if cfg.dtype == "bf16" else "f32")
-                done += 1
-                if time.perf_counter() - t0 >= seconds:
-                    break
-            if time.perf_counter() - t0 >= seconds:
-                break
-        el = time.perf_counter() - t0
-    seq_steps = done / cfg.num_kv_heads
-    return {"value": seq_steps / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{done} (sequence, KV head) rows of the workload = {seq_steps:.2f} "
-                      f"sequence-steps in {el:.1f} s, one thread (numpy, BLAS limited to 1)"}
+        while time.perf_counter() - t0 < seconds:
+            done += _oracle_row(rows[done % len(rows)])
+    return dict(rows=done, seconds=time.perf_counter() - t0)
+
+
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def cpu_baseline(pool: "OraclePool", inp, seconds: float) -> dict:
+    """The CPU oracle on all host cores (one process per core, on the workload's first
+    decode step) and on one thread (on the host state as it stands), on a bounded sample
+    of the workload's rows."""
+    cfg = inp.cfg
+    one = oracle_rate_single(inp, seconds / 3)
+    allc = pool.rate(seconds)
+    H = cfg.num_kv_heads
+    v1 = one["rows"] / H / one["seconds"]
+    va = allc["rows"] / H / allc["seconds"]
+    return {"value": va, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+            "single_thread_value": v1,
+            "sample": f"{allc['rows']} (sequence, KV head) rows of the workload's first decode "
+                      f"step = {allc['rows'] / H:.1f} sequence-steps in {allc['seconds']:.1f} s "
+                      f"on {pool.workers} processes (one thread each, numpy); one thread alone: "
+                      f"{one['rows']} rows in {one['seconds']:.1f} s"}
 
 
 def run_reference(args) -> int:
@@ -238,212 +343,477 @@ def run_reference(args) -> int:
         return 0
     W, cfg = workload(args)
     inp = W.generate(cfg)
-    rows_per_step = max(8, min(cfg.batch * cfg.num_kv_heads, 64))
-    per_step = []
-    for i in range(args.warmup + args.steps):
-        import oracle as O
-        rows = W.sample_rows(cfg, rows_per_step, seed=100 + i)
-        t0 = time.perf_counter()
-        for b, h in rows:
-            rp = W.row_problem(inp, b, h)
-            O.blocktopk_decode(rp["q"], rp["k_pages"], rp["v_pages"], rp["block_table"],
-                               rp["seq_lens"], cfg.sm_scale, cfg.top_k,
-                               store="bf16" if cfg.dtype == "bf16" else "f32")
-        if i >= args.warmup:
-            per_step.append(time.perf_counter() - t0)
-    t = sum(per_step) / len(per_step)
-    seq_steps = rows_per_step / cfg.num_kv_heads
+    pool = OraclePool(inp, host_cores())
+    H = cfg.num_kv_heads
+    per_step_s = 1.0                     # a bounded sample of rows per step
+    times, rows = [], []
+    try:
+        for i in range(args.warmup + args.steps):
+            r = pool.rate(per_step_s, seed=100 + i)
+            if i >= args.warmup:
+                times.append(r["seconds"])
+                rows.append(r["rows"])
+    finally:
+        pool.close()
+    t = sum(times) / len(times)
+    seq_steps = sum(rows) / len(rows) / H
     value = seq_steps / t
+    sample = (f"about {seq_steps:.1f} sequence-steps ({sum(rows) // len(rows)} (sequence, KV "
+              f"head) rows) per step, cycling over a seeded row sample of the workload's "
+              f"first decode step, on {pool.workers} processes (one thread each)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": describe(cfg), "batch": cfg.batch,
-                       "sample_per_step": f"{rows_per_step} (sequence, KV head) rows"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": f"{rows_per_step} rows per step = {seq_steps:.2f} "
-                                       f"sequence-steps, one thread"},
+            "config": {"workload": describe(cfg), "batch": cfg.batch, "sample_per_step": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": pool.workers, "kind": "oracle",
+                             "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
+# ------------------------------------------------------------------------------- GPU
+class Ctx:
+    """Process-wide state of one benchmark run."""
+
+    def __init__(self):
+        import torch
+        import torch.distributed as dist
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        local = int(os.environ.get("LOCAL_RANK", "0"))
+        if self.world > 1:
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        self.dev = torch.device("cuda", local)
+        torch.cuda.set_device(self.dev)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+        self.peak, self.peak_kind = peaks()
+
+    def barrier(self):
+        import torch
+        import torch.distributed as dist
+        torch.cuda.synchronize()
+        if self.world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def job_seconds(self, ms_list) -> float:
+        return max_over_ranks(sum(ms_list) / len(ms_list) / 1e3, self.world, self.dev)
+
+
+class DeviceWorkload:
+    """A workload's decode state on the device: cache, centroids of the complete pages
+    (those the current token just completed excepted: the decode appends them)."""
+
+    def __init__(self, cx, cfg, inp=None):
+        import torch
+        import workloads as W
+        import block_top_sparse_centroid_b300 as K
+        self.cfg = cfg
+        self.inp = inp = inp if inp is not None else W.generate(cfg)
+        dev = cx.dev
+        self.lens0 = [int(x) for x in inp.seq_lens]
+        self.cache = K.PagedKVCache(inp.k_pages.to(dev), inp.v_pages.to(dev))
+        self.q = inp.q.to(dev)
+        self.table = inp.block_table.to(dev)
+        self.seq0 = inp.seq_lens.to(dev)
+        self.seq = self.seq0.clone()
+        self.cents = torch.zeros(self.cache.centroid_shape, dtype=self.q.dtype, device=dev)
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        last = inp.last_pages().tolist()
+        self.just = [int(p) for b, p in enumerate(last) if self.lens0[b] % 16 == 0]
+        before = sorted(set(inp.complete_pages().tolist()) - set(self.just))
+        K.centroids_build(self.cache, self.cents,
+                          page_ids=torch.tensor(before, dtype=torch.int32, device=dev),
+                          err_flag=self.err)
+        self.out = torch.empty_like(self.q)
+        self.ws = K.Workspace(dev)
+        self.wsd = K.Workspace(dev)
+
+    def step_bytes(self, lens, appended: int) -> dict:
+        cfg = self.cfg
+        byt = kv_bytes(cfg, lens)
+        es = 2 if cfg.dtype == "bf16" else 4
+        # the appended centroids: two bf16 codes (or one fp32 value) per element
+        byt["append"] = appended * cfg.num_kv_heads * cfg.head_dim * es * (2 if es == 2 else 1)
+        byt["step"] = byt["kv"] + byt["centroids"] + byt["qo"] + byt["append"]
+        return byt
+
+
+def timed_graphs(cx, step_fns, n_warm: int, n_steps: int):
+    """Capture each decode step into its own CUDA graph (with external event-record nodes
+    around its kernels), then replay: n_warm untimed steps, then exactly n_steps timed
+    ones, cycling over the graphs in order (graph 0 restores the initial state).  The L2 is
+    flushed (a write larger than it) before every step, outside the events.  Returns the
+    per-step event times (ms) and, per step, the index of its graph."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+           for _ in step_fns]
+    for i, fn in enumerate(step_fns):          # eager warm-up of every step
+        cx.flush.zero_()
+        fn(evs[i])
+    torch.cuda.synchronize()
+    graphs = []
+    for i, fn in enumerate(step_fns):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="thread_local"):
+            fn(evs[i])
+        graphs.append(g)
+    n = len(graphs)
+    for i in range(max(n_warm, 1)):
+        cx.flush.zero_()
+        graphs[i % n].replay()
+    cx.barrier()
+    res = dict(step_ms=[], kern_ms=[], write_ms=[], idx=[])
+    for i in range(n_steps):
+        j = i % n
+        cx.flush.zero_()                         # L2 flush, outside the timed events
+        graphs[j].replay()
+        e = evs[j]
+        e[3].synchronize()
+        res["step_ms"].append(e[0].elapsed_time(e[3]))
+        res["kern_ms"].append(e[2].elapsed_time(e[3]))
+        res["write_ms"].append(e[4].elapsed_time(e[5]))
+        res["idx"].append(j)
+    cx.barrier()
+    return res
+
+
+def run_single(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None):
+    """One decode step of a single-step workload, timed as a graph replay."""
+    import torch
+    import block_top_sparse_centroid_b300 as K
+    dw = DeviceWorkload(cx, cfg, inp)
+
+    def step(evs, dense):
+        evs[4].record()
+        evs[5].record()
+        if dense:
+            K.decode_timed(dw.cache, dw.q, dw.table, dw.seq, cfg.sm_scale, evs[:4], dense=True,
+                           out=dw.out, workspace=dw.wsd, err_flag=dw.err)
+        else:
+            K.decode_timed(dw.cache, dw.q, dw.table, dw.seq, cfg.sm_scale, evs[:4],
+                           centroids=dw.cents, top_k=cfg.top_k, out=dw.out, workspace=dw.ws,
+                           err_flag=dw.err, append_final=True)
+
+    clocks = ClockSampler(cx.dev.index)
+    sp = timed_graphs(cx, [lambda e: step(e, False)], n_warm, n_steps)
+    clk = clocks.stop()
+    de = timed_graphs(cx, [lambda e: step(e, True)], n_warm, n_steps) if want_dense else None
+    torch.cuda.synchronize()
+    if int(dw.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(dw.err.item())}")
+    byt = dw.step_bytes(dw.lens0, len(dw.just))
+    r = summarize(cx, cfg, sp, [byt["step"]], de, [byt["dense_kv"] + byt["qo"]])
+    r["clocks"] = clk
+    if want_e2e:
+        r["e2e"] = e2e_single(cx, dw, n_warm, n_steps)
+    return r, dw
+
+
+def summarize(cx, cfg, sp, step_bytes, de, dense_bytes) -> dict:
+    """Rates, roofline and dense comparison from per-step event times."""
+    B = cfg.batch
+    step_s = cx.job_seconds(sp["step_ms"])
+    kern_s = sum(sp["kern_ms"]) / len(sp["kern_ms"]) / 1e3
+    tot_bytes = sum(step_bytes[j] for j in sp["idx"])
+    achieved = tot_bytes / (sum(sp["kern_ms"]) / 1e3) / 1e9
+    r = {"value": whole_job_rate(B, cx.world, step_s), "ms_per_step": step_s * 1e3,
+         "kernel_us": kern_s * 1e6, "bytes_per_step": tot_bytes / len(sp["idx"]),
+         "achieved_gbs": achieved, "frac": achieved / cx.peak,
+         "token_write_us": sum(sp["write_ms"]) / len(sp["write_ms"]) * 1e3,
+         "launches": len(sp["idx"])}
+    if de is not None:
+        dense_s = cx.job_seconds(de["step_ms"])
+        dbytes = sum(dense_bytes[j] for j in de["idx"])
+        r["dense"] = {"ms_per_step": dense_s * 1e3,
+                      "seq_steps_per_s": whole_job_rate(B, cx.world, dense_s),
+                      "hbm_gbs": dbytes / (sum(de["kern_ms"]) / 1e3) / 1e9,
+                      "speedup_blocktopk_over_dense": dense_s / step_s}
+        r["launches"] += len(de["idx"])
+    return r
+
+
+def e2e_single(cx, dw, n_warm, n_steps) -> dict:
+    """The same step through the public API with host buffers: pinned q in, out back."""
+    import torch
+    import block_top_sparse_centroid_b300 as K
+    cfg = dw.cfg
+    stream = torch.cuda.current_stream(cx.dev)
+    q_host = dw.inp.q.clone().pin_memory()
+    out_host = torch.empty_like(dw.inp.q).pin_memory()
+    e_ms = []
+    for i in range(n_warm + n_steps):
+        cx.flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dw.q.copy_(q_host, non_blocking=True)
+        K.blocktopk_decode(dw.cache, dw.q, dw.table, dw.seq, dw.cents, cfg.top_k, cfg.sm_scale,
+                           out=dw.out, workspace=dw.ws, err_flag=dw.err, append_final=True)
+        out_host.copy_(dw.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= n_warm:
+            e_ms.append(e0.elapsed_time(e1))
+    e_s = cx.job_seconds(e_ms)
+    return {"value": whole_job_rate(cfg.batch, cx.world, e_s), "unit": UNIT,
+            "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
+            "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
+            "ms_per_step": e_s * 1e3,
+            "path": "public Python API over the C ABI; pinned host q in, host out back, per "
+                    "step; L2 flushed between steps outside the timed region"}
+
+
+class LoopPlan:
+    """The best-of-N decode loop on the device: every step's tokens, where they go, and
+    the sequence lengths and appended pages of every step (known on the host)."""
+
+    def __init__(self, cx, dw):
+        import torch
+        import workloads as W
+        inp = dw.inp
+        self.q0_host = inp.q.clone()            # step 0's queries (the plan replaces inp.q)
+        plan = W.decode_plan(inp)               # advances the host state to the last step
+        self.n = len(plan)
+        dev = cx.dev
+        cfg = dw.cfg
+        self.q = [dw.q] + [t.q.to(dev) for t in plan[1:]]
+        self.k_new = [None] + [t.k_new.to(dev) for t in plan[1:]]
+        self.v_new = [None] + [t.v_new.to(dev) for t in plan[1:]]
+        self.pages = [None] + [t.pages.to(dev) for t in plan[1:]]
+        self.slots = [None] + [t.slots.to(dev) for t in plan[1:]]
+        self.lens = [list(dw.lens0)]
+        for t in range(1, self.n):
+            self.lens.append([x + 1 for x in self.lens[-1]])
+        self.appended = [sum(1 for L in lens if L % 16 == 0) for lens in self.lens]
+        self.host_tokens = plan
+        self.bytes = [dw.step_bytes(lens, a) for lens, a in zip(self.lens, self.appended)]
+
+
+def run_loop(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None):
+    """The best-of-N loop: step t (t >= 1) writes each sample's new token into its page
+    (torch indexing: the caller's part) and advances seq_lens, then decodes; step 0 decodes
+    the initial state and restores it first, so the steps replay in a cycle."""
+    import torch
+    import block_top_sparse_centroid_b300 as K
+    dw = DeviceWorkload(cx, cfg, inp)
+    lp = LoopPlan(cx, dw)
+
+    def step(t, evs, dense):
+        evs[4].record()
+        if t == 0:
+            dw.seq.copy_(dw.seq0)
+        else:
+            dw.cache.k_pages[lp.pages[t], :, lp.slots[t], :] = lp.k_new[t]
+            dw.cache.v_pages[lp.pages[t], :, lp.slots[t], :] = lp.v_new[t]
+            dw.seq.add_(1)
+        evs[5].record()
+        if dense:
+            K.decode_timed(dw.cache, lp.q[t], dw.table, dw.seq, cfg.sm_scale, evs[:4], dense=True,
+                           out=dw.out, workspace=dw.wsd, err_flag=dw.err)
+        else:
+            K.decode_timed(dw.cache, lp.q[t], dw.table, dw.seq, cfg.sm_scale, evs[:4],
+                           centroids=dw.cents, top_k=cfg.top_k, out=dw.out, workspace=dw.ws,
+                           err_flag=dw.err, append_final=True)
+
+    clocks = ClockSampler(cx.dev.index)
+    sp = timed_graphs(cx, [lambda e, t=t: step(t, e, False) for t in range(lp.n)], n_warm, n_steps)
+    clk = clocks.stop()
+    de = (timed_graphs(cx, [lambda e, t=t: step(t, e, True) for t in range(lp.n)], n_warm, n_steps)
+          if want_dense else None)
+    torch.cuda.synchronize()
+    if int(dw.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(dw.err.item())}")
+    r = summarize(cx, cfg, sp, [b["step"] for b in lp.bytes], de,
+                  [b["dense_kv"] + b["qo"] for b in lp.bytes])
+    r["clocks"] = clk
+    r["unique"] = unique_bytes_step0(cx, dw, lp)
+    if want_e2e:
+        r["e2e"] = e2e_loop(cx, dw, lp, n_warm, n_steps)
+    return r, dw
+
+
+def unique_bytes_step0(cx, dw, lp) -> dict:
+    """Logical and unique (each physical page read once) bytes of the loop's first step,
+    from the kept lists of an untimed decode of the initial state."""
+    import torch
+    import numpy as np
+    import block_top_sparse_centroid_b300 as K
+    cfg = dw.cfg
+    B, H, k = cfg.batch, cfg.num_kv_heads, cfg.top_k
+    dw.seq.copy_(dw.seq0)
+    sel = torch.full((B, H, k), -1, dtype=torch.int32, device=cx.dev)
+    K.blocktopk_decode(dw.cache, lp.q[0], dw.table, dw.seq, dw.cents, k, cfg.sm_scale,
+                       out=dw.out, sel_blocks=sel, workspace=dw.ws, err_flag=dw.err,
+                       append_final=True)
+    sel = sel.cpu().numpy()
+    table = dw.inp.block_table.numpy()
+    es = 2
+    kv_pairs, cent_pairs = {}, set()
+    for b in range(B):
+        L = dw.lens0[b]
+        nb = (L + 15) // 16
+        for h in range(H):
+            for j in sel[b, h]:
+                if j < 0:
+                    continue
+                key = (int(table[b, j]), h)
+                kv_pairs[key] = max(kv_pairs.get(key, 0), min(16, L - 16 * int(j)))
+            if nb > k:
+                for j in range(nb - 1):
+                    cent_pairs.add((int(table[b, j]), h))
+    d = cfg.head_dim
+    uniq = 2 * sum(kv_pairs.values()) * d * es + len(cent_pairs) * d * es + lp.bytes[0]["qo"]
+    return {"logical_bytes": lp.bytes[0]["step"] - lp.bytes[0]["append"],
+            "unique_bytes": uniq,
+            "note": "first decode step without its centroid appends; unique counts each "
+                    "(physical page, KV head) once although several samples read it"}
+
+
+def e2e_loop(cx, dw, lp, n_warm, n_steps) -> dict:
+    """The loop through the public API with host buffers: per step the token's q, k, v and
+    its positions go host -> device from pinned memory, the caller writes k, v into the
+    cache and advances seq_lens, one block top-k decode runs, and out comes back."""
+    import torch
+    import block_top_sparse_centroid_b300 as K
+    cfg = dw.cfg
+    stream = torch.cuda.current_stream(cx.dev)
+    pin = lambda t: t.clone().pin_memory()  # noqa: E731
+    hq = [pin(lp.q0_host if t == 0 else lp.host_tokens[t].q) for t in range(lp.n)]
+    hk = [None] + [pin(lp.host_tokens[t].k_new) for t in range(1, lp.n)]
+    hv = [None] + [pin(lp.host_tokens[t].v_new) for t in range(1, lp.n)]
+    hp = [None] + [pin(lp.host_tokens[t].pages) for t in range(1, lp.n)]
+    hs = [None] + [pin(lp.host_tokens[t].slots) for t in range(1, lp.n)]
+    out_host = torch.empty_like(hq[0]).pin_memory()
+    q_dev = torch.empty_like(dw.q)
+    k_dev = torch.empty_like(lp.k_new[1])
+    v_dev = torch.empty_like(lp.v_new[1])
+    p_dev = torch.empty_like(lp.pages[1])
+    s_dev = torch.empty_like(lp.slots[1])
+    h2d = d2h = 0
+    e_ms = []
+    for i in range(n_warm + n_steps):
+        t = i % lp.n
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q_dev.copy_(hq[t], non_blocking=True)
+        nb_in = hq[t].numel() * hq[t].element_size()
+        if t == 0:
+            dw.seq.copy_(dw.seq0)
+        else:
+            for dst, src in ((k_dev, hk[t]), (v_dev, hv[t]), (p_dev, hp[t]), (s_dev, hs[t])):
+                dst.copy_(src, non_blocking=True)
+                nb_in += src.numel() * src.element_size()
+            dw.cache.k_pages[p_dev, :, s_dev, :] = k_dev
+            dw.cache.v_pages[p_dev, :, s_dev, :] = v_dev
+            dw.seq.add_(1)
+        K.blocktopk_decode(dw.cache, q_dev, dw.table, dw.seq, dw.cents, cfg.top_k, cfg.sm_scale,
+                           out=dw.out, workspace=dw.ws, err_flag=dw.err, append_final=True)
+        out_host.copy_(dw.out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= n_warm:
+            e_ms.append(e0.elapsed_time(e1))
+            h2d += nb_in
+            d2h += out_host.numel() * out_host.element_size()
+    e_s = cx.job_seconds(e_ms)
+    return {"value": whole_job_rate(cfg.batch, cx.world, e_s), "unit": UNIT,
+            "h2d_bytes_per_step": h2d // n_steps, "d2h_bytes_per_step": d2h // n_steps,
+            "ms_per_step": e_s * 1e3,
+            "path": "public Python API over the C ABI, per decode step of the loop: pinned host "
+                    "q, k, v and token positions in, the K/V token write and seq_lens advance "
+                    "(torch indexing), one block top-k decode, out back to pinned host memory"}
+
+
 def main() -> int:
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
-
     import torch
-    import torch.distributed as dist
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-
-    import block_top_sparse_centroid_b300 as K
     W, cfg = workload(args)
-    cfg = replica_config(cfg, rank)
+    cfg = replica_config(cfg, int(os.environ.get("RANK", "0")))
     inp = W.generate(cfg)
-    B, H, Hq, d = cfg.batch, cfg.num_kv_heads, cfg.num_q_heads, cfg.head_dim
-    lens = [int(x) for x in inp.seq_lens]
-
-    cache = K.PagedKVCache(inp.k_pages.to(dev), inp.v_pages.to(dev))
-    q = inp.q.to(dev)
-    table = inp.block_table.to(dev)
-    seq = inp.seq_lens.to(dev)
-    cents = torch.zeros((inp.num_pages, H, d), dtype=q.dtype, device=dev)
-    err = torch.zeros(1, dtype=torch.int32, device=dev)
-    last = inp.last_pages()
-    just = [int(p) for b, p in enumerate(last.tolist()) if lens[b] % 16 == 0]
-    full = set(inp.complete_pages().tolist())
-    before = sorted(full - set(just))
-    K.centroids_build(cache, cents, page_ids=torch.tensor(before, dtype=torch.int32, device=dev),
-                      err_flag=err)
-    just_dev = torch.tensor(just, dtype=torch.int32, device=dev)
-    out = torch.empty_like(q)
-    ws = K.Workspace(dev)
-    wsd = K.Workspace(dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def sparse_step(evs):
-        K.decode_timed(cache, q, table, seq, cfg.sm_scale, evs, centroids=cents,
-                       top_k=cfg.top_k, out=out, workspace=ws, err_flag=err, append_final=True)
-
-    def dense_step(evs):
-        K.decode_timed(cache, q, table, seq, cfg.sm_scale, evs, dense=True, out=out,
-                       workspace=wsd, err_flag=err)
-
-    def timed(step_fn, n_warm, n_steps, launches_per_step):
-        """Warm up eagerly, capture one step into a CUDA graph, then time n_steps replays.
-
-        The graph holds the step's kernel(s) (and any counter memsets) with external event-record
-        nodes around them, so every replay timestamps its own kernels on the device and
-        no host-side marshalling or launch latency falls inside the timed region."""
-        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(4)]
-        for _ in range(n_warm):
-            flush.zero_()
-            step_fn(evs)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            step_fn(evs)
-        for _ in range(n_warm):
-            flush.zero_()
-            graph.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        step_ms, attn_ms, score_ms, sel_ms = [], [], [], []
-        for i in range(n_steps):
-            flush.zero_()                       # L2 flush, outside the timed events
-            graph.replay()
-            evs[3].synchronize()
-            step_ms.append(evs[0].elapsed_time(evs[3]))
-            score_ms.append(evs[0].elapsed_time(evs[1]))
-            sel_ms.append(evs[1].elapsed_time(evs[2]))
-            attn_ms.append(evs[2].elapsed_time(evs[3]))
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        torch.cuda.synchronize()
-        return dict(step_ms=step_ms, attn_ms=attn_ms, score_ms=score_ms, sel_ms=sel_ms,
-                    launches=launches_per_step * n_steps)
-
-    per_step = 1 if cfg.dtype == "bf16" else 3   # fused kernel, or score + select + attention
-    clocks = ClockSampler(dev.index)
-    sp = timed(sparse_step, args.warmup, args.steps, per_step)
-    clk = clocks.stop()
-    de = None if args.no_dense else timed(dense_step, args.warmup, args.steps, 1)
-    torch.cuda.synchronize()
-    if int(err.item()) != 0:
-        raise RuntimeError(f"device error flag {int(err.item())}")
-
-    step_s = max_over_ranks(sum(sp["step_ms"]) / len(sp["step_ms"]) / 1e3, world, dev)
-    value = whole_job_rate(B, world, step_s)
-
-    byt = kv_bytes(cfg, lens)
-    es = 2 if cfg.dtype == "bf16" else 4
-    append_bytes = len(just) * H * d * es      # centroid writes; the keys are already on chip
-    step_bytes = byt["kv"] + byt["centroids"] + byt["qo"] + append_bytes
-    # bf16: one fused kernel does the whole step; fp32: the attention kernel dominates
-    attn_bytes = step_bytes if cfg.dtype == "bf16" else byt["kv"] + byt["qo"]
-    attn_s = statistics.mean(sp["attn_ms"]) / 1e3
-    peak, peak_kind = peaks()
-    achieved = attn_bytes / attn_s / 1e9
+    pool = None
+    if int(os.environ.get("RANK", "0")) == 0 and not args.no_cpu_baseline:
+        pool = OraclePool(inp, host_cores())      # forked before the first CUDA call
+    cx = Ctx()
+    loop = cfg.ctx_kind == "best_of_n" and cfg.steps > 1
+    runner = run_loop if loop else run_single
+    r, dw = runner(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e, inp)
+    cpu = None
+    if pool is not None:
+        try:
+            cpu = cpu_baseline(pool, inp, args.cpu_seconds)
+        finally:
+            pool.close()
     trec = traffic_record(describe(cfg))
+    del dw
+    torch.cuda.empty_cache()
 
-    e2e = None
-    if not args.no_e2e:
-        q_host = inp.q.clone().pin_memory()
-        out_host = torch.empty_like(inp.q).pin_memory()
-        e_ms = []
-        for i in range(args.warmup + args.steps):
-            flush.zero_()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            q.copy_(q_host, non_blocking=True)
-            K.blocktopk_decode(cache, q, table, seq, cents, cfg.top_k, cfg.sm_scale, out=out,
-                               workspace=ws, err_flag=err, append_final=True)
-            out_host.copy_(out, non_blocking=True)
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                e_ms.append(e0.elapsed_time(e1))
-        e_s = max_over_ranks(sum(e_ms) / len(e_ms) / 1e3, world, dev)
-        e2e = {"value": whole_job_rate(B, world, e_s), "unit": UNIT,
-               "h2d_bytes_per_step": q_host.numel() * q_host.element_size(),
-               "d2h_bytes_per_step": out_host.numel() * out_host.element_size(),
-               "ms_per_step": e_s * 1e3,
-               "path": "public Python API over the C ABI; pinned host q in, host out back, "
-                       "per step; L2 flushed between steps outside the timed region"}
+    others = {}
+    if not args.no_others and args.config == 4 and not args.batch:
+        for i in (1, 2, 3):
+            oc = replica_config(W.CONFIGS[i], cx.rank)
+            o, odw = run_single(cx, oc, 5, args.other_steps, not args.no_dense, False)
+            del odw
+            torch.cuda.empty_cache()
+            orec = traffic_record(describe(oc))
+            others[oc.name] = {
+                "workload": describe(oc), "value": o["value"], "unit": UNIT,
+                "ms_per_step": o["ms_per_step"], "steps": args.other_steps,
+                "roofline": {"bound": "hbm", "achieved": o["achieved_gbs"], "peak": cx.peak,
+                             "unit": "GB/s", "frac": o["frac"],
+                             "traffic": orec["dram_bytes_per_launch"] if orec else None,
+                             "bytes_per_launch": o["bytes_per_step"],
+                             "launch_us": o["kernel_us"]},
+                "dense": o.get("dense"), "clocks": o["clocks"]}
+            r["launches"] += o["launches"]
 
+    per_launch_kernel = "fused_decode_kernel" if cfg.dtype == "bf16" else "attn_f32_kernel"
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-        "config": {"workload": describe(cfg), "batch": B, "num_q_heads": Hq,
-                   "num_kv_heads": H, "head_dim": d, "top_k": cfg.top_k,
-                   "context": lens[0] if cfg.ctx_kind == "uniform" else "per-sequence",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "flushed (256 MB write) between timed steps, outside the timed events",
-                   "step": "one block top-k decode call: score, select, split-KV attention with "
-                           "merge, and the centroid append of the pages the current token "
-                           "completed (fused, one kernel for bf16)"},
-        "roofline": {"bound": "hbm", "kernel": "fused_decode_kernel" if cfg.dtype == "bf16" else "attn_f32_kernel",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "bytes_per_launch": attn_bytes,
-                     "launch_us": attn_s * 1e6,
-                     "traffic": (trec["dram_bytes_per_launch"] if trec else None)},
-        "step_hbm": {"bytes": step_bytes, "gbs": step_bytes / step_s / 1e9,
-                     "frac": step_bytes / step_s / 1e9 / peak},
-        "kernels_us": ({"before_kernel": statistics.mean(sp["score_ms"]) * 1e3,
-                        "fused_decode_kernel": attn_s * 1e6} if cfg.dtype == "bf16" else
-                       {"score": statistics.mean(sp["score_ms"]) * 1e3,
-                        "select": statistics.mean(sp["sel_ms"]) * 1e3,
-                        "attention": attn_s * 1e6}),
-        "gpu_launches": sp["launches"] + (e2e is not None) * per_step * args.steps,
-        "clocks": clk,
-        "e2e": e2e,
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": cx.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype,
+        "data": "synthetic",
+        "config": {"workload": describe(cfg), "batch": cfg.batch,
+                   "num_q_heads": cfg.num_q_heads, "num_kv_heads": cfg.num_kv_heads,
+                   "head_dim": cfg.head_dim, "top_k": cfg.top_k,
+                   "decode_steps_per_loop": cfg.steps if loop else 1,
+                   "parallelism": f"replicas x{cx.world}" if cx.world > 1 else "single GPU",
+                   "l2": "flushed (256 MB write) before every timed step, outside the timed "
+                         "events",
+                   "step": ("one decode step of the best-of-N loop: block top-k decode (score, "
+                            "select, split-KV attention with merge) and the centroid append of "
+                            "the pages the step's token completed, one fused kernel; the "
+                            "caller's K/V token write and seq_lens advance run before it, "
+                            "outside its events" if loop else
+                            "one block top-k decode call: score, select, split-KV attention "
+                            "with merge, and the centroid append of the pages the current token "
+                            "completed (fused, one kernel for bf16)")},
+        "roofline": {"bound": "hbm", "kernel": per_launch_kernel, "achieved": r["achieved_gbs"],
+                     "peak": cx.peak, "unit": "GB/s", "frac": r["frac"],
+                     "peak_source": f"{cx.peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": r["bytes_per_step"], "launch_us": r["kernel_us"],
+                     "traffic": trec["dram_bytes_per_launch"] if trec else None},
+        "token_write_us": r["token_write_us"] if loop else None,
+        "gpu_launches": r["launches"] + (args.steps if r.get("e2e") else 0),
+        "clocks": r["clocks"],
+        "e2e": r.get("e2e"),
+        "dense": r.get("dense"),
     }
-    if de is not None:
-        dense_s = max_over_ranks(sum(de["step_ms"]) / len(de["step_ms"]) / 1e3, world, dev)
-        line["dense"] = {"ms_per_step": dense_s * 1e3, "seq_steps_per_s": whole_job_rate(B, world, dense_s),
-                         "hbm_gbs": (byt["dense_kv"] + byt["qo"]) / dense_s / 1e9,
-                         "speedup_blocktopk_over_dense": dense_s / step_s}
-        line["gpu_launches"] += de["launches"]
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(inp, cfg, args.cpu_seconds)
-    if rank == 0:
+    if loop:
+        line["roofline"]["unique_step0"] = r["unique"]
+    if others:
+        line["configs"] = others
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if cx.rank == 0:
         print(json.dumps(line))
-    if world > 1:
+    if cx.world > 1:
+        import torch.distributed as dist
         dist.destroy_process_group()
     return 0
 

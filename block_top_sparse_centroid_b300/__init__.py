@@ -7,9 +7,11 @@ there is no CPU or eager fallback.
 """
 from . import _lib
 from ._lib import KinError, load as load_library
-from .api import (BLOCK, PagedKVCache, Workspace, blocktopk_decode, centroids_append,
-                  centroids_build, decode_timed, dense_decode, workspace_size)
+from .api import (BLOCK, PagedKVCache, PreparedDecode, Workspace, blocktopk_decode,
+                  centroids_append, centroids_build, decode_timed, dense_decode,
+                  prepare_blocktopk_decode, prepare_dense_decode, workspace_size)
 
-__all__ = ["BLOCK", "KinError", "PagedKVCache", "Workspace", "blocktopk_decode",
-           "centroids_append", "centroids_build", "decode_timed", "dense_decode", "workspace_size",
-           "load_library"]
+__all__ = ["BLOCK", "KinError", "PagedKVCache", "PreparedDecode", "Workspace",
+           "blocktopk_decode", "centroids_append", "centroids_build", "decode_timed",
+           "dense_decode", "prepare_blocktopk_decode", "prepare_dense_decode",
+           "workspace_size", "load_library"]

@@ -67,21 +67,25 @@ SIGNATURES = {
 _lib = None
 
 
-def load() -> ctypes.CDLL:
-    """Load libkin.so once; raise if it is missing (build it with the package's build)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    if not os.path.exists(LIB_PATH):
-        raise ImportError(f"{LIB_PATH} is missing: build it with "
+def open_library(path: str) -> ctypes.CDLL:
+    """A libkin build at `path` with every declared signature set (not cached)."""
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
                           "`python -m block_top_sparse_centroid_b300.build`")
-    lib = ctypes.CDLL(LIB_PATH)
+    lib = ctypes.CDLL(path)
     for name, (res, args) in SIGNATURES.items():
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
-    _lib = lib
     return lib
+
+
+def load() -> ctypes.CDLL:
+    """Load libkin.so once; raise if it is missing (build it with the package's build)."""
+    global _lib
+    if _lib is None:
+        _lib = open_library(LIB_PATH)
+    return _lib
 
 
 class KinError(RuntimeError):

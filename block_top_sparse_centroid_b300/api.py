@@ -82,6 +82,14 @@ class PagedKVCache:
     def head_dim(self) -> int:
         return int(self.k_pages.shape[3])
 
+    @property
+    def centroid_shape(self) -> tuple:
+        """Shape of the centroid table: [P, H, d] for fp32 caches; [2, P, H, d] for bf16
+        caches (plane 0: the fp32 mean rounded to bf16, plane 1: its rounding residual
+        rounded to bf16)."""
+        shape = (self.num_pages, self.num_kv_heads, self.head_dim)
+        return (2,) + shape if self.dtype == torch.bfloat16 else shape
+
     def c_struct(self) -> L.KvCache:
         return L.KvCache(_DTYPES[self.dtype], self.num_kv_heads, self.head_dim, BLOCK,
                          self.num_pages, self.k_pages.data_ptr(), self.v_pages.data_ptr())
@@ -146,7 +154,7 @@ def centroids_build(cache: PagedKVCache, centroids: Optional[torch.Tensor] = Non
     """Mean key of every listed page (all pages when page_ids is None): kin_centroids_build."""
     lib = L.load()
     dev = cache.device
-    shape = (cache.num_pages, cache.num_kv_heads, cache.head_dim)
+    shape = cache.centroid_shape
     if centroids is None:
         centroids = torch.empty(shape, dtype=cache.dtype, device=dev)
     _need(centroids, "centroids", shape, cache.dtype, dev)
@@ -168,8 +176,7 @@ def centroids_append(cache: PagedKVCache, page_ids: torch.Tensor, centroids: tor
     """Mean key of pages a decode step just completed: kin_centroids_append."""
     lib = L.load()
     dev = cache.device
-    _need(centroids, "centroids", (cache.num_pages, cache.num_kv_heads, cache.head_dim),
-          cache.dtype, dev)
+    _need(centroids, "centroids", cache.centroid_shape, cache.dtype, dev)
     if page_ids.dim() != 1:
         raise ValueError("page_ids must be 1-D")
     _need(page_ids, "page_ids", (page_ids.numel(),), torch.int32, dev)
@@ -181,62 +188,120 @@ def centroids_append(cache: PagedKVCache, page_ids: torch.Tensor, centroids: tor
     return centroids
 
 
+class PreparedDecode:
+    """A decode call whose tensors are fixed: shapes, dtypes and devices are checked and the
+    C structs built once, so that each call only enqueues the kernels (kin_blocktopk_decode
+    or kin_dense_decode).  It keeps every tensor it was given alive.  For a decode loop whose
+    buffers stay the same from step to step (q, out, the cache, the block table and
+    seq_lens updated in place), this is the low-overhead way to call the library.
+
+    stream: a torch stream baked into the call, or None for the current stream of the
+    cache's device at each call."""
+
+    def __init__(self, mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale,
+                 top_k, centroids=None, out=None, lse=None, sel_blocks=None, scores=None,
+                 workspace: Optional[Workspace] = None, err_flag=None, append_final=False,
+                 stream=None):
+        lib = L.load()
+        dev = cache.device
+        if q.dim() != 3:
+            raise ValueError("q must be [batch, num_q_heads, head_dim]")
+        B, Hq, d = (int(x) for x in q.shape)
+        H = cache.num_kv_heads
+        _need(q, "q", (B, Hq, cache.head_dim), cache.dtype, dev)
+        if block_table.dim() != 2:
+            raise ValueError("block_table must be [batch, max_blocks]")
+        maxb = int(block_table.shape[1])
+        _need(block_table, "block_table", (B, maxb), torch.int32, dev)
+        _need(seq_lens, "seq_lens", (B,), torch.int32, dev)
+        if out is None:
+            out = torch.empty_like(q)
+        _need(out, "out", (B, Hq, d), cache.dtype, dev)
+        if lse is not None:
+            _need(lse, "lse", (B, Hq), torch.float32, dev)
+        if mode == L.MODE_BLOCKTOPK or append_final:
+            if centroids is None:
+                raise ValueError("centroids are required")
+            _need(centroids, "centroids", cache.centroid_shape, cache.dtype, dev)
+        if mode == L.MODE_BLOCKTOPK:
+            if sel_blocks is not None:
+                _need(sel_blocks, "sel_blocks", (B, H, top_k), torch.int32, dev)
+            if scores is not None:
+                _need(scores, "scores", (B, H, maxb), torch.float32, dev)
+        a = L.DecodeArgs()
+        a.batch, a.num_q_heads, a.max_blocks, a.top_k = B, Hq, maxb, int(top_k)
+        a.sm_scale = float(sm_scale)
+        a.q, a.block_table, a.seq_lens = q.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr()
+        a.centroids = centroids.data_ptr() if (centroids is not None and
+                                               (mode == L.MODE_BLOCKTOPK or append_final)) else None
+        a.flags = L.KIN_DECODE_APPEND_FINAL if append_final else 0
+        a.out = out.data_ptr()
+        a.lse = None if lse is None else lse.data_ptr()
+        a.sel_blocks = None if (sel_blocks is None or mode != L.MODE_BLOCKTOPK) else sel_blocks.data_ptr()
+        a.scores = None if (scores is None or mode != L.MODE_BLOCKTOPK) else scores.data_ptr()
+        c = cache.c_struct()
+        need = ctypes.c_size_t(0)
+        L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a), mode, ctypes.byref(need)),
+                "kin_workspace_size")
+        ws = _workspace(dev, int(need.value), workspace)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
+        a.err_flag = None if err_flag is None else _err_ptr(err_flag, dev).value
+        self._keep = (cache, q, block_table, seq_lens, centroids, out, lse, sel_blocks, scores,
+                      ws, err_flag)
+        self._lib, self._c, self._a, self._mode, self._dev = lib, c, a, mode, dev
+        self._cref, self._aref = ctypes.byref(c), ctypes.byref(a)
+        self._fn = lib.kin_blocktopk_decode if mode == L.MODE_BLOCKTOPK else lib.kin_dense_decode
+        self._name = "kin_blocktopk_decode" if mode == L.MODE_BLOCKTOPK else "kin_dense_decode"
+        self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+        self.out = out
+
+    def __call__(self, stream=None) -> torch.Tensor:
+        st = self._stream if stream is None and self._stream is not None else _stream(stream, self._dev)
+        L.check(self._fn(self._cref, self._aref, st), self._name)
+        return self.out
+
+    def timed(self, events, stream=None) -> torch.Tensor:
+        """The same call through kin_decode_timed, recording 4 torch.cuda.Events."""
+        st = self._stream if stream is None and self._stream is not None else _stream(stream, self._dev)
+        handles = (ctypes.c_void_p * 4)(*[_event_handle(e, stream, self._dev) for e in events])
+        L.check(self._lib.kin_decode_timed(self._cref, self._aref, self._mode, handles, st),
+                "kin_decode_timed")
+        return self.out
+
+
 def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, top_k,
             centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream, events=None,
             append_final=False):
-    lib = L.load()
-    dev = cache.device
-    if q.dim() != 3:
-        raise ValueError("q must be [batch, num_q_heads, head_dim]")
-    B, Hq, d = (int(x) for x in q.shape)
-    H = cache.num_kv_heads
-    _need(q, "q", (B, Hq, cache.head_dim), cache.dtype, dev)
-    if block_table.dim() != 2:
-        raise ValueError("block_table must be [batch, max_blocks]")
-    maxb = int(block_table.shape[1])
-    _need(block_table, "block_table", (B, maxb), torch.int32, dev)
-    _need(seq_lens, "seq_lens", (B,), torch.int32, dev)
-    if out is None:
-        out = torch.empty_like(q)
-    _need(out, "out", (B, Hq, d), cache.dtype, dev)
-    if lse is not None:
-        _need(lse, "lse", (B, Hq), torch.float32, dev)
-    if mode == L.MODE_BLOCKTOPK or append_final:
-        if centroids is None:
-            raise ValueError("centroids are required")
-        _need(centroids, "centroids", (cache.num_pages, H, d), cache.dtype, dev)
-    if mode == L.MODE_BLOCKTOPK:
-        if sel_blocks is not None:
-            _need(sel_blocks, "sel_blocks", (B, H, top_k), torch.int32, dev)
-        if scores is not None:
-            _need(scores, "scores", (B, H, maxb), torch.float32, dev)
-    a = L.DecodeArgs()
-    a.batch, a.num_q_heads, a.max_blocks, a.top_k = B, Hq, maxb, int(top_k)
-    a.sm_scale = float(sm_scale)
-    a.q, a.block_table, a.seq_lens = q.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr()
-    a.centroids = centroids.data_ptr() if (centroids is not None and
-                                           (mode == 0 or append_final)) else None
-    a.flags = L.KIN_DECODE_APPEND_FINAL if append_final else 0
-    a.out = out.data_ptr()
-    a.lse = None if lse is None else lse.data_ptr()
-    a.sel_blocks = None if (sel_blocks is None or mode != 0) else sel_blocks.data_ptr()
-    a.scores = None if (scores is None or mode != 0) else scores.data_ptr()
-    c = cache.c_struct()
-    need = ctypes.c_size_t(0)
-    L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a), mode, ctypes.byref(need)),
-            "kin_workspace_size")
-    ws = _workspace(dev, int(need.value), workspace)
-    a.workspace, a.workspace_bytes = ws.data_ptr(), ws.numel()
-    a.err_flag = None if err_flag is None else _err_ptr(err_flag, dev).value
+    call = PreparedDecode(mode, cache, q, block_table, seq_lens, sm_scale, top_k, centroids,
+                          out, lse, sel_blocks, scores, workspace, err_flag, append_final)
     if events is not None:
-        handles = (ctypes.c_void_p * 4)(*[_event_handle(e, stream, dev) for e in events])
-        L.check(lib.kin_decode_timed(ctypes.byref(c), ctypes.byref(a), mode, handles,
-                                     _stream(stream, dev)), "kin_decode_timed")
-        return out
-    fn = lib.kin_blocktopk_decode if mode == L.MODE_BLOCKTOPK else lib.kin_dense_decode
-    L.check(fn(ctypes.byref(c), ctypes.byref(a), _stream(stream, dev)),
-            "kin_blocktopk_decode" if mode == L.MODE_BLOCKTOPK else "kin_dense_decode")
-    return out
+        return call.timed(list(events), stream)
+    return call(stream)
+
+
+def prepare_blocktopk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                             seq_lens: torch.Tensor, centroids: torch.Tensor, top_k: int,
+                             sm_scale: float, out: Optional[torch.Tensor] = None,
+                             lse: Optional[torch.Tensor] = None,
+                             sel_blocks: Optional[torch.Tensor] = None,
+                             scores: Optional[torch.Tensor] = None,
+                             workspace: Optional[Workspace] = None,
+                             err_flag: Optional[torch.Tensor] = None,
+                             append_final: bool = False, stream=None) -> PreparedDecode:
+    """A block top-k decode call (kin_blocktopk_decode) prepared once, run by calling it."""
+    return PreparedDecode(L.MODE_BLOCKTOPK, cache, q, block_table, seq_lens, sm_scale, top_k,
+                          centroids, out, lse, sel_blocks, scores, workspace, err_flag,
+                          append_final, stream)
+
+
+def prepare_dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                         seq_lens: torch.Tensor, sm_scale: float,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         workspace: Optional[Workspace] = None,
+                         err_flag: Optional[torch.Tensor] = None, stream=None) -> PreparedDecode:
+    """A dense decode call (kin_dense_decode) prepared once, run by calling it."""
+    return PreparedDecode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, None,
+                          out, lse, None, None, workspace, err_flag, False, stream)
 
 
 def _event_handle(ev: "torch.cuda.Event", stream, dev) -> int:

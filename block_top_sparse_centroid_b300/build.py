@@ -1,6 +1,10 @@
 """Build libkin.so (the C-ABI CUDA library) in-tree for sm_103a with nvcc.
 
-Usage:  python -m block_top_sparse_centroid_b300.build [--force] [--verbose]
+Usage:  python -m block_top_sparse_centroid_b300.build [--force] [--verbose] [--variant NAME]
+
+Variants are test builds of the same sources with other compile-time limits, written next
+to the library as libkin_<name>.so: "shortwait" gives every bounded wait of the kernels
+4096 tries instead of about four million, so that a test can make a wait run out quickly.
 """
 from __future__ import annotations
 
@@ -14,6 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkin.so")
+VARIANTS = {"shortwait": ["-DKIN_MAX_WAIT_TRIES=4096u"]}
 
 SOURCES = ["centroid.cu", "score_select.cu", "attention.cu", "decode_fused.cu", "kin_api.cu",
            "noalloc.cu"]
@@ -28,21 +33,27 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libkin")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(PKG, f"libkin_{variant}.so")
+
+
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS] + [os.path.join(INCLUDE, "kin.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every source into libkin.so next to this file; returns its path."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, variant: str = "") -> str:
+    """Compile every source into libkin.so (or a test variant) next to this file; returns
+    its path."""
+    lib = lib_path(variant)
+    if not force and not _stale(lib):
+        return lib
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--shared", "-Xcompiler", "-fPIC",
            "-Xcompiler", "-fvisibility=hidden", "-I", INCLUDE, "-I", CSRC,
-           "-o", LIB + ".tmp"]
+           *VARIANTS.get(variant, []), "-o", lib + ".tmp"]
     if verbose:
         cmd += ["-Xptxas", "-v"]
     cmd += [os.path.join(CSRC, f) for f in SOURCES]
@@ -50,11 +61,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if verbose or res.returncode != 0:
         sys.stderr.write(res.stdout + res.stderr)
     if res.returncode != 0:
-        raise RuntimeError("nvcc failed building libkin.so")
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+        raise RuntimeError(f"nvcc failed building {os.path.basename(lib)}")
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose="--verbose" in sys.argv)
-    print(LIB)
+    var = sys.argv[sys.argv.index("--variant") + 1] if "--variant" in sys.argv else ""
+    print(build(force="--force" in sys.argv, verbose="--verbose" in sys.argv, variant=var))

@@ -5,9 +5,12 @@
 // One block is one 16-token KV page (Kinetics README, "Benchmark Block TopK Attention
 // throughput").
 //
-// c[p, h, :] = (sum_{t=0..15} K[p, h, t, :]) * (1/16), summed in fp32 in ascending t,
-// stored in the cache dtype (bf16 round-to-nearest-even).  HBM-bound: 16*d elements in,
-// d out per (page, head).  Each thread owns one 16-byte column slice of the page and
+// c[p, h, :] = (sum_{t=0..15} K[p, h, t, :]) * (1/16), summed in fp32 in ascending t.
+// fp32 caches store c.  bf16 caches store two bf16 codes per element in two planes of the
+// table: plane 0 holds c rounded to bf16 (round-to-nearest-even), plane 1 the residual
+// c - plane 0 (exact in fp32) rounded to bf16, so that plane 0 + plane 1 is c to about
+// 2^-16 of its size.  HBM-bound: 16*d elements in, d (fp32) or 2d (bf16) out per
+// (page, head).  Each thread owns one 16-byte column slice of the page and
 // walks the 16 rows, so every element is accumulated by one thread in token order; the
 // 16 row loads are issued back to back for memory-level parallelism.
 #include "kin_common.cuh"
@@ -50,7 +53,16 @@ __global__ void __launch_bounds__(256) centroid_kernel(const T *__restrict__ k_p
 #pragma unroll
   for (int i = 0; i < kVec; ++i) acc[i] = __fmul_rn(acc[i], 1.0f / kBlock);
   T *dst = cents + (page * H + h) * D + slice * kVec;
-  *reinterpret_cast<uint4 *>(dst) = Elem<T>::pack(acc);
+  const uint4 code = Elem<T>::pack(acc);
+  *reinterpret_cast<uint4 *>(dst) = code;
+  if constexpr (sizeof(T) == 2) {
+    // plane 1: the residual of the rounding, itself rounded to bf16
+    float hi[kVec];
+    Elem<T>::unpack(code, hi);
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) acc[i] = __fsub_rn(acc[i], hi[i]);
+    *reinterpret_cast<uint4 *>(dst + num_pages * H * D) = Elem<T>::pack(acc);
+  }
 }
 
 template <typename T, int D>

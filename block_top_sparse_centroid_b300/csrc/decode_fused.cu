@@ -43,6 +43,7 @@
 // smallest queue index can always progress.  The last CTA to finish zeroes the workspace
 // counters for the next call.
 #include <atomic>
+#include <type_traits>
 
 #include "attn_common.cuh"
 #include "kin_internal.h"
@@ -150,17 +151,24 @@ struct FusedShared {
   int score_arrive[16];         // consumers: warps done with a score item (kScoreSlots)
   int flag;                     // consumers: last-arriver flag of the split merge
   int sel_done;                 // consumers: select items finished (read by the queue leader)
+  int sel_ok;                   // consumers: the current select item's scores arrived
   int last_cta;                 // this CTA finished last (clears the counters)
   int abort;                    // set after a wait of this CTA timed out
 };
 
 // Bounded mbarrier wait.  After any wait of the CTA has timed out (a broken protocol),
 // later waits give up within a few hundred polls, so the CTA winds down quickly instead
-// of timing out wait by wait.
+// of timing out wait by wait.  The waits that hand out work descriptors (deliver = true)
+// are the exception: they never take that shortcut and have a 16 times longer bound,
+// because every warp of the CTA must see the same items in the same order (the consumer
+// warps' group barriers inside an item are reached by all of them only then), and after a
+// timeout the queue leader still delivers every descriptor promptly (its other waits end
+// early).
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, FusedShared &sh,
-                                         int32_t *err) {
+                                         int32_t *err, bool deliver = false) {
   const uint32_t addr = smem_u32(bar);
-  for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+  const uint32_t tries = deliver ? 16u * kMaxWaitTries : kMaxWaitTries;
+  for (uint32_t i = 0; i < tries; ++i) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
@@ -170,7 +178,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, FusedSh
         : "r"(addr), "r"(parity)
         : "memory");
     if (done) return true;
-    if ((i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0) return false;
+    if (!deliver && (i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0)
+      return false;
   }
   *reinterpret_cast<volatile int *>(&sh.abort) = 1;
   flag_error(err, KIN_DEVERR_TIMEOUT);
@@ -261,19 +270,527 @@ __device__ __forceinline__ uint32_t score_key(float s) {
   return s != s ? 0u : k;
 }
 
-// Kept blocks of one row, by one warp: {nb-1} plus the m largest of the n scores
-// srow[0..n) (equal scores to the lower index), ascending, into out[0..m].  keys: room for
-// n words of shared memory, or NULL (every pass then re-reads srow); hist: 256 words.
-__device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *keys, int *hist,
-                            int32_t *out, int lane) {
-  if (keys != nullptr) {
-    for (int j = lane; j < n; j += 32) keys[j] = score_key(__ldcg(srow + j));
-    __syncwarp();
+// The score of a key (inverse of score_key for keys of numbers).
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// ----------------------------------------------------------------------------------
+// Selection.  The kernel scores every candidate with the first centroid code (bf16), which
+// is what it can stream at full bandwidth; the reference ranking is by the fp32 mean.  With
+// E >= |s - s*| for every candidate of the row (p.bound) and T the m-th largest score s, a
+// candidate with s > T + 2E is in the top m by s* as well (only candidates with s > T, at
+// most m - 1 of them, can beat it), and one with s < T - 2E is out (every candidate with
+// s >= T, at least m of them, beats it).  The candidates in between ("ambiguous") are
+// re-scored with both codes, s + qs . c2, which is the score of the fp32 mean to about
+// 2^-16 of its size, and the m - (number in) best of them are kept, equal scores to the
+// lower block index.  The selection runs on modified keys: in -> kKeyIn, out -> 0,
+// ambiguous -> the key of the re-scored value, so that one top-m search over them yields
+// the kept list.  Keys of real scores are >= 2, padding slots 0.
+// ----------------------------------------------------------------------------------
+constexpr uint32_t kKeyIn = 0xffffffffu;   // above the key of every number (+inf: 0xff800000)
+// Ambiguous candidates a selecting warp (a cooperative CTA) lists and re-scores at once.
+constexpr int kAmbCapWarp = 256;
+constexpr int kAmbCapCta = 1024;
+
+struct Window {
+  uint32_t lo, hi;   // in: key > hi; ambiguous: lo <= key <= hi; out: key < lo
+  bool refine;       // ambiguous candidates are re-scored (else they tie, lower index first)
+};
+
+// The window around the m-th largest key t for the row bound E.  Without a usable bound (a
+// non-finite T or E) the window is t itself: candidates tied at t, taken in index order.
+__device__ __forceinline__ Window make_window(uint32_t t, float E) {
+  const float T = key_score(t);
+  if (t < 2u || !(fabsf(T) <= 3.0e38f) || !(E >= 0.f && E <= 1.0e37f)) return Window{t, t, false};
+  const float e2 = 2.f * E;
+  return Window{max(score_key(__fadd_rd(T, -e2)), 2u), score_key(__fadd_ru(T, e2)), true};
+}
+
+// What the re-scoring of a row's ambiguous candidates needs.
+struct RefineCtx {
+  const __nv_bfloat16 *c2;     // second centroid code of KV head h: page p at c2 + p * stride
+  const int32_t *trow;         // block-table row of the sequence
+  int64_t stride;              // H * D
+  int64_t num_pages;
+  const float *qs;             // group-summed query of the row, fp32 [D] (shared memory)
+};
+
+// Key of the re-scored candidate j with first-code score s: s + qs . c2_j, computed by LPC
+// consecutive lanes (each one D / LPC slice of the dimensions; every lane of the group
+// returns the key).  All loads of a lane are issued before any is used.
+template <int D, int LPC>
+__device__ __forceinline__ uint32_t refined_key(const RefineCtx &rc, int j, float s, int lane) {
+  constexpr int kChunks = D / 8 / LPC;   // 16-byte chunks per lane
+  const int part = lane % LPC;
+  const int pg = __ldg(rc.trow + j);
+  float corr = 0.f;
+  if (pg >= 0 && pg < rc.num_pages) {
+    const uint4 *src = reinterpret_cast<const uint4 *>(rc.c2 + pg * rc.stride) + part * kChunks;
+    uint4 raw[kChunks];
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) raw[c] = __ldcg(src + c);
+    const float *qs = rc.qs + part * kChunks * 8;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      float f[8];
+      Elem<__nv_bfloat16>::unpack(raw[c], f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) corr = fmaf(qs[8 * c + k], f[k], corr);
+    }
   }
-  auto key_at = [&](int j) -> uint32_t {
-    return keys != nullptr ? keys[j] : score_key(__ldcg(srow + j));
+#pragma unroll
+  for (int o = 1; o < LPC; o <<= 1) corr += __shfl_xor_sync(0xffffffffu, corr, o);
+  return max(score_key(s + corr), 2u);
+}
+
+// Group-summed query of KV head h (sum over g in order, fp32) into qs[0..D), by one warp:
+// lane l sums dimensions [l D / 32, (l + 1) D / 32), one vector load per query head; the
+// loop is unrolled so that several heads' loads are in flight at once.
+template <int D>
+__device__ __forceinline__ void group_query(const __nv_bfloat16 *qg, int G, float *qs, int lane) {
+  constexpr int kPer = D / 32;                     // 4 (D = 128) or 2 (D = 64)
+  using Raw = typename std::conditional<kPer == 4, uint2, uint32_t>::type;
+  auto unpack = [](const Raw &r, float (&f)[kPer]) {
+    if constexpr (kPer == 4) {
+      f[0] = bf16_lo(r.x); f[1] = bf16_hi(r.x); f[2] = bf16_lo(r.y); f[3] = bf16_hi(r.y);
+    } else {
+      f[0] = bf16_lo(r); f[1] = bf16_hi(r);
+    }
+  };
+  const Raw *src = reinterpret_cast<const Raw *>(qg + lane * kPer);
+  float acc[kPer];
+  unpack(__ldg(src), acc);
+#pragma unroll 4
+  for (int g = 1; g < G; ++g) {
+    float f[kPer];
+    unpack(__ldg(src + g * (D / kPer)), f);
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) acc[i] += f[i];
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) qs[lane * kPer + i] = acc[i];
+}
+
+// Re-score the n_amb listed ambiguous candidates (lj) into lr by the NTHR threads
+// ti = 0 .. NTHR - 1, one candidate per thread at a time: its first-code score is read back
+// from the row's scores alongside its page.  In a one-warp selection the caller's key
+// registers are dead by then (only the class ballots are needed afterwards), which leaves
+// room for a row's loads in flight.
+template <int D, int NTHR>
+__device__ __forceinline__ void refine_listed(const RefineCtx &rc, const float *srow, const int *lj,
+                                              uint32_t *lr, int n_amb, int ti, int lane) {
+  for (int e = ti; e < n_amb; e += NTHR) {
+    const int j = lj[e];
+    const float s = __ldcg(srow + j);
+    lr[e] = refined_key<D, 1>(rc, j, s, lane);
+  }
+}
+
+// m-th largest of the keys held in registers by one warp (lane l: slots i, candidate
+// l + 32 i; 0 = padding or out): t, and whether exactly m keys are >= t.  Built bit by bit
+// from the highest bit where the nonzero keys differ: a bit stays set when at least m keys
+// are >= the candidate prefix; the search stops once exactly m keys are >= the prefix (those
+// are the m largest, and nothing outside them ties with anything inside).
+template <int KPL>
+__device__ __forceinline__ uint32_t bits_threshold(const uint32_t (&key)[KPL], int m, bool &exact) {
+  uint32_t all_and = 0xffffffffu, all_or = 0u;
+  int nz = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    all_and &= key[i] != 0u ? key[i] : 0xffffffffu;
+    all_or |= key[i];
+    nz += key[i] != 0u ? 1 : 0;
+  }
+  all_and = __reduce_and_sync(0xffffffffu, all_and);
+  all_or = __reduce_or_sync(0xffffffffu, all_or);
+  nz = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(nz)));
+  const uint32_t diff = all_and ^ all_or;
+  const int top = diff == 0u ? 0 : 32 - __clz(diff);   // bits [0, top) undecided
+  uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
+  // keys >= t: every nonzero key shares the bits above `top` (t = 0 only while the search
+  // runs: the callers have more than m nonzero keys, so the last bit sets t >= 1)
+  int cnt_t = nz;
+#pragma unroll 1
+  for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
+    const uint32_t cand = t | (1u << b);
+    int c0 = 0, c1 = 0;
+#pragma unroll
+    for (int i = 0; i + 1 < KPL; i += 2) {
+      c0 += key[i] >= cand ? 1 : 0;
+      c1 += key[i + 1] >= cand ? 1 : 0;
+    }
+    const int c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
+    if (c >= m) {
+      t = cand;
+      cnt_t = c;
+    }
+  }
+  exact = cnt_t == m;
+  return t;
+}
+
+// Index-order compaction of the m kept candidates: every key > t, plus (exact: the keys
+// equal to t too; else the first m - count(key > t) keys equal to t in index order).
+// jbase: candidate index of slot 0 of lane 0; out[pos0 ..] receives the warp's kept
+// candidates, eq0 equal keys are already taken by earlier warps, take_eq in total.
+template <int KPL>
+__device__ __forceinline__ void bits_emit(const uint32_t (&key)[KPL], uint32_t t, bool exact,
+                                          int take_eq, int pos0, int eq0, int m, int jbase,
+                                          int32_t *out, int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int written = pos0, eq_seen = eq0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {   // unrolled: key[] stays in registers
+    unsigned km = __ballot_sync(0xffffffffu, exact ? key[i] >= t : key[i] > t);
+    if (!exact) {
+      const unsigned eqm = __ballot_sync(0xffffffffu, key[i] == t);
+      const int eq_here = __popc(eqm);
+      int eq_take = take_eq - eq_seen;
+      if (eq_take >= eq_here) {
+        km |= eqm;
+      } else if (eq_take > 0) {   // the first eq_take of this slot
+        unsigned msk = eqm;
+        for (; eq_take > 0; --eq_take) {
+          const unsigned low = msk & (0u - msk);
+          km |= low;
+          msk ^= low;
+        }
+      }
+      eq_seen += eq_here;
+    }
+    const int pos = written + __popc(km & lt);
+    if (((km >> lane) & 1u) && pos < m) out[pos] = jbase + lane + 32 * i;
+    written += __popc(km);
+  }
+}
+
+// Classify the warp's register keys against the window: for every slot i, the ballots of
+// its in and ambiguous candidates go to bal[i] and bal[KPL + i] (shared memory, written by
+// lane 0), so that the later passes over the candidates run as short loops over the
+// ballots instead of long unrolled code over the registers.  Returns the warp's counts.
+template <int KPL>
+__device__ __forceinline__ void classify(const uint32_t (&key)[KPL], const Window &w,
+                                         uint32_t *bal, int &n_in, int &n_amb, int lane) {
+  int a = 0, b = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const unsigned bi = __ballot_sync(0xffffffffu, key[i] > w.hi);
+    const unsigned ba = __ballot_sync(0xffffffffu, key[i] >= w.lo && key[i] <= w.hi);
+    if (lane == 0) {
+      bal[i] = bi;
+      bal[KPL + i] = ba;
+    }
+    a += __popc(bi);
+    b += __popc(ba);
+  }
+  n_in = a;
+  n_amb = b;
+  __syncwarp();
+}
+
+// List the ambiguous candidates of slots 0 .. nslots - 1 with rank (in index order over the
+// whole row) in [0, cap) into lj.  Ranks of this warp start at rank0; slot i, lane l holds
+// candidate jbase + l + 32 i.
+__device__ __forceinline__ void list_amb(const uint32_t *bal, int nslots, int rank0, int cap,
+                                         int jbase, int *lj, int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int base = rank0;
+  for (int i = 0; i < nslots; ++i) {
+    const unsigned ba = bal[nslots + i];
+    const int rank = base + __popc(ba & lt);
+    if (((ba >> lane) & 1u) && rank < cap) lj[rank] = jbase + lane + 32 * i;
+    base += __popc(ba);
+  }
+}
+
+// Choose r of the na listed ambiguous candidates (ranks 0 .. na - 1, in index order) by
+// one warp: the r largest re-scored keys lr[], equal keys to the lower rank.  Sets lf[rank]
+// (1 = kept) for every rank.  KA keys per lane: na <= 32 KA.
+template <int KA>
+__device__ __forceinline__ void choose_amb(const uint32_t *lr, int na, int r, uint8_t *lf,
+                                           int lane) {
+  uint32_t key[KA];
+#pragma unroll
+  for (int i = 0; i < KA; ++i) key[i] = lane + 32 * i < na ? lr[lane + 32 * i] : 0u;
+  bool exact;
+  const uint32_t t = bits_threshold<KA>(key, r, exact);
+  int take_eq = 0;
+  if (!exact) {
+    int g = 0;
+#pragma unroll
+    for (int i = 0; i < KA; ++i) g += key[i] > t ? 1 : 0;
+    take_eq = r - static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g)));
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  int eq_seen = 0;
+#pragma unroll
+  for (int i = 0; i < KA; ++i) {
+    const bool eq = !exact && key[i] == t;
+    const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+    const bool keep = exact ? key[i] >= t : (key[i] > t || (eq && eq_seen + __popc(eqm & lt) < take_eq));
+    if (lane + 32 * i < na) lf[lane + 32 * i] = keep ? 1 : 0;
+    eq_seen += __popc(eqm);
+  }
+}
+
+// Index-order compaction from the class ballots (classify): a candidate is kept when it
+// is in, or ambiguous and chosen (lf[rank] != 0; lf == NULL: every ambiguous one).  Ranks
+// of this warp's ambiguous candidates start at rank0; its kept candidates go to out[pos0 ..].
+__device__ __forceinline__ void emit_kept(const uint32_t *bal, int nslots, const uint8_t *lf,
+                                          int rank0, int pos0, int m, int jbase, int32_t *out,
+                                          int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int base = rank0, written = pos0;
+  for (int i = 0; i < nslots; ++i) {
+    const unsigned bi = bal[i], ba = bal[nslots + i];
+    const bool a = ((ba >> lane) & 1u) != 0;
+    const int rank = base + __popc(ba & lt);
+    const bool keep = ((bi >> lane) & 1u) != 0 || (a && (lf == nullptr || lf[rank] != 0));
+    const unsigned km = __ballot_sync(0xffffffffu, keep);
+    const int pos = written + __popc(km & lt);
+    if (keep && pos < m) out[pos] = jbase + lane + 32 * i;
+    written += __popc(km);
+    base += __popc(ba);
+  }
+}
+
+// This warp's kept count under the class ballots and flags (see emit_kept).
+__device__ __forceinline__ int kept_count(const uint32_t *bal, int nslots, const uint8_t *lf,
+                                          int rank0, int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int base = rank0, c = 0;
+  for (int i = 0; i < nslots; ++i) {
+    const unsigned bi = bal[i], ba = bal[nslots + i];
+    const bool keep = ((bi >> lane) & 1u) != 0 ||
+                      (((ba >> lane) & 1u) != 0 && lf[base + __popc(ba & lt)] != 0);
+    c += __popc(__ballot_sync(0xffffffffu, keep));
+    base += __popc(ba);
+  }
+  return c;
+}
+
+// Scratch of one selecting warp (or of the CTA in a cooperative selection).
+struct SelScratch {
+  float *qs;      // [D]
+  int *lj;        // [cap] listed ambiguous candidates
+  uint32_t *lr;   // [cap] their re-scored keys
+  uint8_t *lf;    // [cap] 1 = kept
+  uint32_t *bal;  // [2 * slots] class ballots of the warp (cooperative: per warp)
+  int *hist;      // [256] radix histograms (rows too long for the registers)
+  int *xs;        // [128] cross-warp partial sums (cooperative selection)
+};
+
+template <int D>
+__device__ void warp_select_long(const float *srow, int n, int m, int nb, float E,
+                                 const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
+                                 const SelScratch &ss, int32_t *out, int lane);
+
+// Kept blocks of one row by one warp, keys in registers: lane l holds candidates
+// j = l + 32 i, i < KPL (n <= 32 KPL).  out[0..m) = the m kept candidates ascending,
+// out[m] = nb - 1.  After the window classifies the candidates, only the class masks and
+// the listed ambiguous candidates are needed: the registers of the keys are free for the
+// re-scoring loads.
+template <int KPL, int D>
+__device__ void warp_select_bits(const float *srow, int n, int m, int nb, float E,
+                                 const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
+                                 const SelScratch &ss, int32_t *out, int lane KIN_TRACE_PARAM) {
+  KIN_TIC(t_k);
+  uint32_t key[KPL];
+  const int nv = n > lane ? (n - lane + 31) / 32 : 0;   // this lane's candidates
+  {
+    float sv[KPL];   // every load issued before any is used
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) sv[i] = i < nv ? __ldcg(srow + lane + 32 * i) : 0.f;
+    // the group-summed query for a re-scoring, while the scores are in flight
+    group_query<D>(qg, G, const_cast<float *>(rc.qs), lane);
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 2u) : 0u;
+  }
+  KIN_TOC(kTrCSelKeys, t_k);
+  if (m > 0) {
+    KIN_TIC(t_p);
+    bool exact;
+    const uint32_t t = bits_threshold<KPL>(key, m, exact);
+    const Window w = make_window(t, E);
+    int n_in, n_amb;
+    classify<KPL>(key, w, ss.bal, n_in, n_amb, lane);
+    const int r = m - n_in;
+    if (n_amb == r) {              // every ambiguous candidate is kept: no re-scoring
+      emit_kept(ss.bal, KPL, nullptr, 0, 0, m, 0, out, lane);
+    } else if (n_amb > kAmbCapWarp) {
+      // more ambiguous candidates than the list holds (clustered scores): the exact
+      // selection that re-reads the row instead of holding it
+      warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+      return;
+    } else {
+      list_amb(ss.bal, KPL, 0, kAmbCapWarp, 0, ss.lj, lane);
+      __syncwarp();
+      if (w.refine) {
+        refine_listed<D, 32>(rc, srow, ss.lj, ss.lr, n_amb, lane, lane);
+      } else {
+        for (int e = lane; e < n_amb; e += 32) ss.lr[e] = 2u;
+      }
+      __syncwarp();
+      if (n_amb <= 32 * 2)
+        choose_amb<2>(ss.lr, n_amb, r, ss.lf, lane);
+      else
+        choose_amb<kAmbCapWarp / 32>(ss.lr, n_amb, r, ss.lf, lane);
+      __syncwarp();
+      emit_kept(ss.bal, KPL, ss.lf, 0, 0, m, 0, out, lane);
+    }
+    KIN_TOC(kTrCSelPass, t_p);
+  }
+  if (lane == 0) out[m] = nb - 1;
+}
+
+// Selection of one row by all NW consumer warps: warp w holds candidates
+// j = w 32 KPL + 32 i + lane (i < KPL), keys in registers; n <= NW 32 KPL.  The same steps
+// as warp_select_bits, with each count summed over the warps through shared memory (a
+// per-warp partial, double-buffered by parity, one consumer-group barrier per sum).  The
+// kept list is written in index order: each warp offsets its own compaction by the counts
+// of the warps before it.
+template <int KPL, int NW, int D, typename Bar>
+__device__ void cta_select_row(const float *srow, int n, int m, int nb, float E,
+                               const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
+                               const SelScratch &ss, int32_t *out) {
+  constexpr int kCap = kAmbCapCta;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int jbase = w * 32 * KPL;
+  uint32_t key[KPL];
+  {
+    float sv[KPL];
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      const int j = jbase + lane + 32 * i;
+      sv[i] = j < n ? __ldcg(srow + j) : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) key[i] = jbase + lane + 32 * i < n ? max(score_key(sv[i]), 2u) : 0u;
+  }
+  int *xs = ss.xs;
+  int par = 0;
+  // sum of v over the consumer warps (v must be warp-uniform); *before = the sum over the
+  // warps before this one
+  auto cta_sum = [&](int v, int *before) -> int {
+    if (lane == 0) xs[par * NW + w] = v;
+    Bar::sync();
+    int s = 0, b = 0;
+#pragma unroll
+    for (int u = 0; u < NW; ++u) {
+      const int x = xs[par * NW + u];
+      s += x;
+      b += u < w ? x : 0;
+    }
+    par ^= 1;
+    if (before != nullptr) *before = b;
+    return s;
+  };
+  // m-th largest key over the CTA (same bit search as bits_threshold)
+  auto threshold = [&](bool &exact) -> uint32_t {
+    uint32_t a = 0xffffffffu, o = 0u;
+    int nz = 0;
+#pragma unroll
+    for (int i = 0; i < KPL; ++i) {
+      a &= key[i] != 0u ? key[i] : 0xffffffffu;
+      o |= key[i];
+      nz += key[i] != 0u ? 1 : 0;
+    }
+    a = __reduce_and_sync(0xffffffffu, a);
+    o = __reduce_or_sync(0xffffffffu, o);
+    nz = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(nz)));
+    if (lane == 0) {
+      xs[64 + w] = static_cast<int>(a);
+      xs[64 + NW + w] = static_cast<int>(o);
+    }
+    const int nz_all = cta_sum(nz, nullptr);   // its barrier also publishes a and o
+    uint32_t all_and = 0xffffffffu, all_or = 0u;
+#pragma unroll
+    for (int u = 0; u < NW; ++u) {
+      all_and &= static_cast<uint32_t>(xs[64 + u]);
+      all_or |= static_cast<uint32_t>(xs[64 + NW + u]);
+    }
+    const uint32_t diff = all_and ^ all_or;
+    const int top = diff == 0u ? 0 : 32 - __clz(diff);
+    uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
+    int cnt_t = nz_all;
+#pragma unroll 1
+    for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
+      const uint32_t cand = t | (1u << b);
+        int c0 = 0, c1 = 0;
+#pragma unroll
+      for (int i = 0; i + 1 < KPL; i += 2) {
+        c0 += key[i] >= cand ? 1 : 0;
+        c1 += key[i + 1] >= cand ? 1 : 0;
+      }
+      const int cw = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
+      const int c = cta_sum(cw, nullptr);
+      if (c >= m) {
+        t = cand;
+        cnt_t = c;
+      }
+    }
+    Bar::sync();   // xs[64 ..] is rewritten by the next search
+    exact = cnt_t == m;
+    return t;
   };
   if (m > 0) {
+    bool exact;
+    const uint32_t t = threshold(exact);
+    const Window win = make_window(t, E);
+    uint32_t *bal = ss.bal + w * 2 * KPL;   // this warp's class ballots
+    int n_in_w, n_amb_w;
+    classify<KPL>(key, win, bal, n_in_w, n_amb_w, lane);
+    int in_before;
+    const int n_in = cta_sum(n_in_w, &in_before);
+    int amb_before;
+    const int n_amb = cta_sum(n_amb_w, &amb_before);
+    const int r = m - n_in;
+    if (n_amb == r) {
+      // every ambiguous candidate is kept: this warp's kept ones follow the earlier warps'
+      emit_kept(bal, KPL, nullptr, amb_before, in_before + amb_before, m, jbase, out, lane);
+    } else if (n_amb > kCap) {
+      // more ambiguous candidates than the list holds: warp 0 selects the row exactly,
+      // re-reading it from L2
+      if (w == 0) warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+      return;
+    } else {
+      if (win.refine && w == 0) group_query<D>(qg, G, const_cast<float *>(rc.qs), lane);
+      list_amb(bal, KPL, amb_before, kCap, jbase, ss.lj, lane);
+      Bar::sync();   // the list and qs complete
+      if (win.refine) {
+        refine_listed<D, NW * 32>(rc, srow, ss.lj, ss.lr, n_amb, threadIdx.x, lane);
+      } else {
+        for (int e = threadIdx.x; e < n_amb; e += NW * 32) ss.lr[e] = 2u;
+      }
+      Bar::sync();
+      if (w == 0) {
+        if (n_amb <= 32 * 4)
+          choose_amb<4>(ss.lr, n_amb, r, ss.lf, lane);
+        else
+          choose_amb<kCap / 32>(ss.lr, n_amb, r, ss.lf, lane);
+      }
+      Bar::sync();
+      int kept_before;
+      cta_sum(kept_count(bal, KPL, ss.lf, amb_before, lane), &kept_before);
+      emit_kept(bal, KPL, ss.lf, amb_before, kept_before, m, jbase, out, lane);
+    }
+  }
+  if (threadIdx.x == 0) out[m] = nb - 1;
+}
+
+// Kept blocks of one row by one warp for rows too long for the registers: radix select
+// (8-bit digits, shared histogram) that re-reads the row from L2 on every pass, first on
+// the first-code keys (for the window), then on the modified keys, whose ambiguous
+// candidates are re-scored wherever a pass meets them.
+template <int D>
+__device__ void warp_select_long(const float *srow, int n, int m, int nb, float E,
+                                 const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
+                                 const SelScratch &ss, int32_t *out, int lane) {
+  int *hist = ss.hist;
+  // m-th largest key of key_at(0 .. n) (keys >= 1 where counted) and how many keys equal
+  // to it are kept
+  auto radix = [&](auto key_at, uint32_t &thr, int &take_eq) {
     uint32_t prefix = 0u, mask = 0u;
     int remaining = m;               // keys still to take at or below the current prefix
 #pragma unroll 1
@@ -320,15 +837,42 @@ __device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *k
       mask |= 255u << shift;
       __syncwarp();
     }
-    const uint32_t thr = prefix;     // key of the m-th largest score
-    const int take_eq = remaining;   // keys equal to thr that are kept (>= 1)
+    thr = prefix;
+    take_eq = remaining;
+  };
+  auto first_key = [&](int j) -> uint32_t { return max(score_key(__ldcg(srow + j)), 2u); };
+  if (m > 0) {
+    uint32_t t;
+    int take_eq;
+    radix(first_key, t, take_eq);
+    const Window w = make_window(t, E);
+    int n_in = 0, n_amb = 0;
+    for (int j = lane; j < n; j += 32) {
+      const uint32_t k = first_key(j);
+      n_in += k > w.hi ? 1 : 0;
+      n_amb += (k >= w.lo && k <= w.hi) ? 1 : 0;
+    }
+    n_in = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n_in)));
+    n_amb = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(n_amb)));
+    if (w.refine && n_amb != m - n_in) group_query<D>(qg, G, const_cast<float *>(rc.qs), lane);
+    __syncwarp();
+    const bool every_amb = n_amb == m - n_in;
+    auto mod_key = [&](int j) -> uint32_t {
+      const float s = __ldcg(srow + j);
+      const uint32_t k = max(score_key(s), 2u);
+      if (k > w.hi) return kKeyIn;
+      if (k < w.lo) return 0u;
+      if (every_amb) return kKeyIn;
+      return w.refine ? refined_key<D, 1>(rc, j, s, lane) : 2u;
+    };
+    radix(mod_key, t, take_eq);
     const unsigned lt = (1u << lane) - 1u;
     int written = 0, eq_seen = 0;
     for (int base = 0; base < n; base += 32) {
       const int j = base + lane;
-      const uint32_t key = j < n ? key_at(j) : 0u;
-      const bool gt = j < n && key > thr;
-      const bool eq = j < n && key == thr;
+      const uint32_t key = j < n ? mod_key(j) : 0u;
+      const bool gt = j < n && key > t;
+      const bool eq = j < n && key == t;
       const unsigned eqm = __ballot_sync(0xffffffffu, eq);
       const bool keep = gt || (eq && eq_seen + __popc(eqm & lt) < take_eq);
       const unsigned km = __ballot_sync(0xffffffffu, keep);
@@ -341,225 +885,11 @@ __device__ void warp_select(const float *srow, int n, int m, int nb, uint32_t *k
   if (lane == 0) out[m] = nb - 1;
 }
 
-// The same selection with the row's keys in registers (lane l holds candidates
-// j = l + 32 i, i < KPL; n <= 32 KPL) and no shared memory.  The m-th largest key T is
-// built bit by bit from the highest bit where the keys differ: a bit stays set when at
-// least m keys are >= the candidate (independent compares per lane, one warp sum).  The
-// search stops early once exactly m keys are >= the prefix built so far: those are the
-// m largest, and no key outside them equals one inside.  Otherwise (T is tied) every
-// key > T is kept, and the first m - count(key > T) keys equal to T in index order.
-// Padding slots hold key 0 and real keys are at least 1 (NaN maps to 1), so no per-key
-// step needs a validity test.
-template <int KPL>
-__device__ void warp_select_bits(const float *srow, int n, int m, int nb, int32_t *out,
-                                 int lane KIN_TRACE_PARAM) {
-  KIN_TIC(t_k);
-  uint32_t key[KPL];
-  const int nv = n > lane ? (n - lane + 31) / 32 : 0;   // this lane's candidates
-  {
-    float sv[KPL];   // every load issued before any is used
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) sv[i] = i < nv ? __ldcg(srow + lane + 32 * i) : 0.f;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 1u) : 0u;
-  }
-  KIN_TOC(kTrCSelKeys, t_k);
-  const unsigned lt = (1u << lane) - 1u;
-  if (m > 0) {
-    KIN_TIC(t_p);
-    uint32_t all_and = 0xffffffffu, all_or = 0u;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      all_and &= key[i] != 0u ? key[i] : 0xffffffffu;
-      all_or |= key[i];
-    }
-    all_and = __reduce_and_sync(0xffffffffu, all_and);
-    all_or = __reduce_or_sync(0xffffffffu, all_or);
-    const uint32_t diff = all_and ^ all_or;
-    const int top = diff == 0u ? 0 : 32 - __clz(diff);   // bits [0, top) undecided
-    uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
-    int cnt_t = n;   // keys >= t: every real key shares the bits above `top`
-#pragma unroll 1
-    for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
-      const uint32_t cand = t | (1u << b);
-      int c0 = 0, c1 = 0;
-#pragma unroll
-      for (int i = 0; i < KPL; i += 2) {
-        c0 += key[i] >= cand ? 1 : 0;
-        c1 += key[i + 1] >= cand ? 1 : 0;
-      }
-      const int c = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
-      if (c >= m) {
-        t = cand;
-        cnt_t = c;
-      }
-    }
-    KIN_TOC(kTrCSelPass, t_p);
-    if (cnt_t == m) {
-      // the keys >= t are exactly the m largest: index-order compaction of one vote each
-      unsigned km[KPL];
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) km[i] = __ballot_sync(0xffffffffu, key[i] >= t);
-      int written = 0;
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) {
-        if ((km[i] >> lane) & 1u) out[written + __popc(km[i] & lt)] = lane + 32 * i;
-        written += __popc(km[i]);
-      }
-    } else {
-      // t is the m-th largest key and is tied
-      int g0 = 0;
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) g0 += key[i] > t ? 1 : 0;
-      const int take_eq =
-          m - static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g0)));
-      int written = 0, eq_seen = 0;
-#pragma unroll
-      for (int i = 0; i < KPL; ++i) {   // unrolled: key[] stays in registers
-        unsigned km = __ballot_sync(0xffffffffu, key[i] > t);
-        const unsigned eqm = __ballot_sync(0xffffffffu, key[i] == t);
-        const int eq_here = __popc(eqm);
-        int eq_take = take_eq - eq_seen;                    // equal keys still to take
-        if (eq_take >= eq_here) {
-          km |= eqm;
-        } else if (eq_take > 0) {                           // the first eq_take of this row
-          unsigned msk = eqm;
-          for (; eq_take > 0; --eq_take) {
-            const unsigned low = msk & (0u - msk);
-            km |= low;
-            msk ^= low;
-          }
-        }
-        const int pos = written + __popc(km & lt);
-        if (((km >> lane) & 1u) && pos < m) out[pos] = lane + 32 * i;
-        written += __popc(km);
-        eq_seen += eq_here;
-      }
-    }
-  }
-  if (lane == 0) out[m] = nb - 1;
-}
-
-// Selection of one row by all NW consumer warps: warp w holds candidates
-// j = w 32 KPL + 32 i + lane (i < KPL), keys in registers; n <= NW 32 KPL.  The same
-// bit-by-bit search as warp_select_bits, with each pass's count summed over the warps
-// through shared memory (a per-warp partial, double-buffered by pass parity, one
-// consumer-group barrier per pass), and the same early exit.  The kept list is written in
-// index order: each warp offsets its own compaction by the counts of the warps before it.
-// xs: 64 words of shared scratch.
-template <int KPL, int NW, typename Bar>
-__device__ void cta_select_row(const float *srow, int n, int m, int nb, int32_t *out, int *xs) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int jbase = w * 32 * KPL + lane;
-  uint32_t key[KPL];
-  {
-    float sv[KPL];
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) sv[i] = jbase + 32 * i < n ? __ldcg(srow + jbase + 32 * i) : 0.f;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) key[i] = jbase + 32 * i < n ? max(score_key(sv[i]), 1u) : 0u;
-  }
-  const unsigned lt = (1u << lane) - 1u;
-  int *pass_cnt = xs;           // [2][NW]
-  int *and_or = xs + 2 * NW;    // [2][NW]
-  int *wtot = xs + 4 * NW;      // [2][NW]
-  if (m > 0) {
-    uint32_t a = 0xffffffffu, o = 0u;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      a &= key[i] != 0u ? key[i] : 0xffffffffu;
-      o |= key[i];
-    }
-    a = __reduce_and_sync(0xffffffffu, a);
-    o = __reduce_or_sync(0xffffffffu, o);
-    if (lane == 0) {
-      and_or[w] = static_cast<int>(a);
-      and_or[NW + w] = static_cast<int>(o);
-    }
-    Bar::sync();
-    uint32_t all_and = 0xffffffffu, all_or = 0u;
-#pragma unroll
-    for (int v = 0; v < NW; ++v) {
-      all_and &= static_cast<uint32_t>(and_or[v]);
-      all_or |= static_cast<uint32_t>(and_or[NW + v]);
-    }
-    const uint32_t diff = all_and ^ all_or;
-    const int top = diff == 0u ? 0 : 32 - __clz(diff);
-    uint32_t t = top == 32 ? 0u : (all_and & (0xffffffffu << top));
-    int cnt_t = n;
-    int par = 0;
-#pragma unroll 1
-    for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
-      const uint32_t cand = t | (1u << b);
-      int c0 = 0, c1 = 0;
-#pragma unroll
-      for (int i = 0; i < KPL; i += 2) {
-        c0 += key[i] >= cand ? 1 : 0;
-        c1 += key[i + 1] >= cand ? 1 : 0;
-      }
-      const int cw = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(c0 + c1)));
-      if (lane == 0) pass_cnt[par * NW + w] = cw;
-      Bar::sync();
-      int c = 0;
-#pragma unroll
-      for (int v = 0; v < NW; ++v) c += pass_cnt[par * NW + v];
-      par ^= 1;
-      if (c >= m) {
-        t = cand;
-        cnt_t = c;
-      }
-    }
-    // this warp's kept keys (and, when t is tied, its keys equal to t)
-    const bool exact = cnt_t == m;
-    int g = 0, e = 0;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      g += exact ? (key[i] >= t ? 1 : 0) : (key[i] > t ? 1 : 0);
-      e += (!exact && key[i] == t) ? 1 : 0;
-    }
-    g = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(g)));
-    e = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(e)));
-    if (lane == 0) {
-      wtot[w] = g;
-      wtot[NW + w] = e;
-    }
-    Bar::sync();
-    int g_before = 0, e_before = 0, g_all = 0;
-#pragma unroll
-    for (int v = 0; v < NW; ++v) {
-      g_all += wtot[v];
-      if (v < w) {
-        g_before += wtot[v];
-        e_before += wtot[NW + v];
-      }
-    }
-    const int take_eq = exact ? 0 : m - g_all;   // equal keys kept, lowest indices first
-    int written = g_before + min(e_before, take_eq), eq_seen = e_before;
-#pragma unroll
-    for (int i = 0; i < KPL; ++i) {
-      unsigned km = __ballot_sync(0xffffffffu, exact ? key[i] >= t : key[i] > t);
-      if (!exact) {
-        const unsigned eqm = __ballot_sync(0xffffffffu, key[i] == t);
-        const int eq_here = __popc(eqm);
-        int eq_take = take_eq - eq_seen;
-        if (eq_take >= eq_here) {
-          km |= eqm;
-        } else if (eq_take > 0) {
-          unsigned msk = eqm;
-          for (; eq_take > 0; --eq_take) {
-            const unsigned low = msk & (0u - msk);
-            km |= low;
-            msk ^= low;
-          }
-        }
-        eq_seen += eq_here;
-      }
-      const int pos = written + __popc(km & lt);
-      if (((km >> lane) & 1u) && pos < m) out[pos] = jbase + 32 * i;
-      written += __popc(km);
-    }
-  }
-  if (threadIdx.x == 0) out[m] = nb - 1;
+// The kept list of a row whose selection could not run (its scores never arrived): the
+// first m candidates and the final block, so that the attention reads valid pages.  Only
+// written after a timeout, which the error flag reports.
+__device__ __forceinline__ void fallback_kept(int m, int nb, int32_t *out, int ti, int nthr) {
+  for (int i = ti; i <= m; i += nthr) out[i] = i < m ? i : nb - 1;
 }
 
 // ----------------------------------------------------------------------------------
@@ -757,7 +1087,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       if (lane == 0) {
         const int slot = nd % kDescs;
         KIN_TIC(t0);
-        wait_bar(&sh.dempty[slot], ((nd / kDescs) & 1u) ^ 1u, sh, p.err);
+        wait_bar(&sh.dempty[slot], ((nd / kDescs) & 1u) ^ 1u, sh, p.err, true);
         KIN_TOC(kTrPPush, t0);
         sh.desc[slot] = d;
         mbar_arrive(&sh.dfull[slot]);
@@ -765,7 +1095,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       __syncwarp();
     }
     const int slot = nd % kDescs;
-    if (!wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err)) break;
+    if (!wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err, true)) break;
     const Desc d = sh.desc[slot];
     ++nd;
     if (d.kind == kDescScore) {
@@ -937,15 +1267,12 @@ struct QRegs {
 template <int D, int QS>
 __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<D> &qr,
                                               const float *qs, int hs, int nc, uint32_t vmask,
-                                              int lane) {
+                                              int lane, float &norm2) {
   constexpr int kPer = D / 32;
+  const uint8_t *own = stage + lane * (D * 2);   // centroid `lane`'s row of the stage
   stage += lane * kPer * 2;
   qs += lane * kPer;
-  float v[32];
-  int hh = 0, pi = 0;
-#pragma unroll
-  for (int cc = 0; cc < 32; ++cc) {
-    float f[kPer], qv[kPer];
+  auto unpack = [&](int cc, float (&f)[kPer]) {
     if constexpr (kPer == 4) {
       const uint2 raw = *reinterpret_cast<const uint2 *>(stage + cc * (D * 2));
       f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
@@ -953,6 +1280,44 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
       const uint32_t raw = *reinterpret_cast<const uint32_t *>(stage + cc * (D * 2));
       f[0] = bf16_lo(raw); f[1] = bf16_hi(raw);
     }
+  };
+  // bit cc: centroid cc of the stage is scored (present and its page valid)
+  uint32_t vm = 0u;
+  {
+    int hh = 0, pi = 0;
+#pragma unroll
+    for (int cc = 0; cc < 32; ++cc) {
+      const int page = QS > 0 ? cc / QS : pi;
+      vm |= static_cast<uint32_t>(cc < nc && ((vmask >> page) & 1u)) << cc;
+      if constexpr (QS == 0) {
+        if (++hh == hs) {
+          hh = 0;
+          ++pi;
+        }
+      }
+    }
+  }
+  auto valid = [&](int cc) { return ((vm >> cc) & 1u) != 0; };
+  // 32 partial sums, one per centroid, reduced so that lane c ends with centroid c's sum
+  auto butterfly = [&](float (&v)[32]) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      const bool upper = (lane & o) != 0;
+#pragma unroll
+      for (int k = 0; k < o; ++k) {
+        const float send = upper ? v[k] : v[k + o];
+        const float keep = upper ? v[k + o] : v[k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    return v[0];
+  };
+  float v[32];
+  int hh = 0;
+#pragma unroll
+  for (int cc = 0; cc < 32; ++cc) {
+    float f[kPer], qv[kPer];
+    unpack(cc, f);
     if constexpr (QS > 0) {
 #pragma unroll
       for (int i = 0; i < kPer; ++i) qv[i] = qr.v[cc % QS][i];
@@ -966,26 +1331,28 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
     float acc = 0.f;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) acc = fmaf(qv[i], f[i], acc);
-    const int page = QS > 0 ? cc / QS : pi;
-    v[cc] = (cc < nc && ((vmask >> page) & 1u)) ? acc : 0.f;
+    v[cc] = valid(cc) ? acc : 0.f;
     if constexpr (QS == 0) {
-      if (++hh == hs) {
-        hh = 0;
-        ++pi;
-      }
+      if (++hh == hs) hh = 0;
     }
   }
+  const float score = butterfly(v);
+  // lane c: the squared norm of centroid c from its own row, 16-byte chunks in an order
+  // rotated by the lane (rows are 2 D bytes apart, so 8 consecutive lanes read 8 distinct
+  // bank groups)
+  float nrm = 0.f;
+  if (valid(lane)) {
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      float f[8];
+      Elem<__nv_bfloat16>::unpack(
+          *reinterpret_cast<const uint4 *>(own + ((c + lane) & (D / 8 - 1)) * 16), f);
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int k = 0; k < o; ++k) {
-      const float send = upper ? v[k] : v[k + o];
-      const float keep = upper ? v[k + o] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      for (int k = 0; k < 8; ++k) nrm = fmaf(f[k], f[k], nrm);
     }
   }
-  return v[0];
+  norm2 = nrm;
+  return score;
 }
 
 // Score of the centroids of one ring stage for ranges of exactly 8 heads: four lanes per
@@ -1022,44 +1389,65 @@ __device__ __forceinline__ void load_qslice(const float *qs, int lane, QSlice<D>
 template <int D>
 __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSlice<D> &qv, int np,
                                                 uint32_t vmask, float *srow_base, int64_t sstride,
-                                                int jst, int lane) {
+                                                int jst, int lane, float &norm2_max) {
   constexpr int kCh = D / 32;
   const int head = lane >> 2, part = lane & 3, rot = h8_rot<D>(lane);
   const uint8_t *base = stage + head * (D * 2) + part * (D / 4) * 2;
-  float acc[4];
+  float acc[4], nrm[4];
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {   // pages of the stage (loads unconditional)
     const uint8_t *row = base + pp * 8 * (D * 2);
-    float a0 = 0.f, a1 = 0.f;
+    float a0 = 0.f, a1 = 0.f, n0 = 0.f, n1 = 0.f;
 #pragma unroll
     for (int c = 0; c < kCh; ++c) {
       const uint4 raw = *reinterpret_cast<const uint4 *>(row + ((c + rot) & (kCh - 1)) * 16);
-      a0 = fmaf(qv.v[c * 8 + 0], bf16_lo(raw.x), a0);
-      a1 = fmaf(qv.v[c * 8 + 1], bf16_hi(raw.x), a1);
-      a0 = fmaf(qv.v[c * 8 + 2], bf16_lo(raw.y), a0);
-      a1 = fmaf(qv.v[c * 8 + 3], bf16_hi(raw.y), a1);
-      a0 = fmaf(qv.v[c * 8 + 4], bf16_lo(raw.z), a0);
-      a1 = fmaf(qv.v[c * 8 + 5], bf16_hi(raw.z), a1);
-      a0 = fmaf(qv.v[c * 8 + 6], bf16_lo(raw.w), a0);
-      a1 = fmaf(qv.v[c * 8 + 7], bf16_hi(raw.w), a1);
+      float f[8];
+      f[0] = bf16_lo(raw.x); f[1] = bf16_hi(raw.x); f[2] = bf16_lo(raw.y); f[3] = bf16_hi(raw.y);
+      f[4] = bf16_lo(raw.z); f[5] = bf16_hi(raw.z); f[6] = bf16_lo(raw.w); f[7] = bf16_hi(raw.w);
+#pragma unroll
+      for (int k = 0; k < 8; k += 2) {
+        a0 = fmaf(qv.v[c * 8 + k], f[k], a0);
+        a1 = fmaf(qv.v[c * 8 + k + 1], f[k + 1], a1);
+        n0 = fmaf(f[k], f[k], n0);
+        n1 = fmaf(f[k + 1], f[k + 1], n1);
+      }
     }
     acc[pp] = a0 + a1;
+    nrm[pp] = n0 + n1;
   }
 #pragma unroll
   for (int pp = 0; pp < 4; ++pp) {
     acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], 1);
     acc[pp] += __shfl_xor_sync(0xffffffffu, acc[pp], 2);
+    nrm[pp] += __shfl_xor_sync(0xffffffffu, nrm[pp], 1);
+    nrm[pp] += __shfl_xor_sync(0xffffffffu, nrm[pp], 2);
   }
   if (part == 0) {
     float *dst = srow_base + head * sstride + jst;
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp)
-      if (pp < np) __stcg(dst + pp, ((vmask >> pp) & 1u) ? acc[pp] : -INFINITY);
+    for (int pp = 0; pp < 4; ++pp) {
+      const bool valid = pp < np && ((vmask >> pp) & 1u);
+      if (pp < np) __stcg(dst + pp, valid ? acc[pp] : -INFINITY);
+      if (valid) norm2_max = fmaxf(norm2_max, nrm[pp]);
+    }
   }
 }
 
+// Upper bound of |s - s*| for every candidate of a row, where s is the group score the
+// kernel computes from the first centroid code c1 (bf16) and s* the exact score of the
+// fp32 mean c: |c_i - c1_i| <= 2^-8 |c1_i| (round to nearest, 8 significant bits), so
+// |s - s*| <= 2^-8 sum_i |qs_i| |c1_i| <= 2^-8 |qs|_2 |c1|_2 (Cauchy-Schwarz), plus fp32
+// rounding of the products, sums and of qs itself (below 2^-16 of the same quantity, for
+// d <= 128 and G <= 16).  kBoundScale = 2^-8 + 2^-12 covers both; the 1e-30 term covers
+// subnormal codes, whose error is absolute.
+constexpr float kBoundScale = 0.00415039062f;   // 2^-8 + 2^-12, exact in fp32
+__device__ __forceinline__ float row_bound(float qn2, float cn2) {
+  return kBoundScale * sqrtf(qn2) * (sqrtf(cn2) + 1e-30f);
+}
+
 // The warp's ring stages of one score item (stages t = q, q + kProducers, ... of the item,
-// those with j % kPPC == c): wait for each, score its centroids, store them, free it.
+// those with j % kPPC == c): wait for each, score its centroids, store them, free it.  Also
+// raises each row's error bound (p.bound) to cover the centroids this warp scored.
 template <int D, int NT, int QS>
 __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d, uint8_t *ring,
                                              const float *qs, FusedShared &sh, uint32_t &n
@@ -1072,13 +1460,25 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
   const int b = d.row, h0 = d.x0, hs = d.x2;
   QRegs<D> qr;
   QSlice<D> qv;
+  float qn2 = 0.f;           // |qs|^2 of the lane's head
+  float cn2 = -1.f;          // largest |c1|^2 the lane scored (-1: none)
+  int head;                  // the lane's head within the range
   if constexpr (QS == 8) {
     load_qslice<D>(qs, lane, qv);
-  } else if constexpr (QS > 0) {
 #pragma unroll
-    for (int hh = 0; hh < QS; ++hh)
+    for (int i = 0; i < D / 4; ++i) qn2 = fmaf(qv.v[i], qv.v[i], qn2);
+    qn2 += __shfl_xor_sync(0xffffffffu, qn2, 1);
+    qn2 += __shfl_xor_sync(0xffffffffu, qn2, 2);
+    head = lane >> 2;
+  } else {
+    if constexpr (QS > 0) {
 #pragma unroll
-      for (int i = 0; i < D / 32; ++i) qr.v[hh][i] = qs[hh * D + lane * (D / 32) + i];
+      for (int hh = 0; hh < QS; ++hh)
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) qr.v[hh][i] = qs[hh * D + lane * (D / 32) + i];
+    }
+    head = lane % hs;
+    for (int i = 0; i < D; ++i) qn2 = fmaf(qs[head * D + i], qs[head * D + i], qn2);
   }
   for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
     if (j % C::kPPC != c) continue;
@@ -1095,19 +1495,24 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
     if constexpr (QS == 8) {
       stage_scores_h8<D>(ring + s * R::kStageBytes, qv, ok ? np : 0, vmask,
                          p.scores + static_cast<int64_t>(b * H + h0) * p.max_blocks, p.max_blocks,
-                         jst, lane);
+                         jst, lane, cn2);
     } else {
-      const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane);
+      float nrm;
+      const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane, nrm);
       if (lane < nc) {
         const int pl = lane / hs, hl = lane % hs;
+        const bool valid = ((vmask >> pl) & 1u) != 0;
         __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
-               ((vmask >> pl) & 1u) ? score : -INFINITY);
+               valid ? score : -INFINITY);
+        if (valid) cn2 = fmaxf(cn2, nrm);
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sh.empty[s]);
     KIN_TOC(kTrCScoreComp, t_sc);
   }
+  // bounds are non-negative, so their fp32 bit patterns order like the values
+  if (cn2 >= 0.f) atomicMax(p.bound + b * H + h0 + head, __float_as_uint(row_bound(qn2, cn2)));
 }
 
 template <int D, int NT>
@@ -1193,41 +1598,77 @@ __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring
   if (d.first < 0) C::Bar::sync();   // the shared group-summed queries are reused next item
 }
 
+// Selection scratch: per selecting warp (one warp per row) kSelWarpBytes of the consumer
+// scratch; a cooperative selection uses the start of it for the whole CTA.
+constexpr int kSelWarpBytes = 4352;
+static_assert(8 * kSelWarpBytes <= kScratchBytes, "per-warp selection scratch");
+static_assert(kSelWarpBytes % 16 == 0, "aligned per-warp regions");
+
+template <int D>
+__device__ __forceinline__ SelScratch sel_scratch(uint8_t *base, int cap, bool coop) {
+  SelScratch ss;
+  ss.xs = reinterpret_cast<int *>(base);                               // 128 ints
+  ss.qs = reinterpret_cast<float *>(base + 512);                       // D floats
+  ss.lj = reinterpret_cast<int *>(base + 512 + D * 4);                 // cap
+  ss.lr = reinterpret_cast<uint32_t *>(base + 512 + D * 4 + cap * 4);  // cap
+  ss.lf = base + 512 + D * 4 + cap * 8;                                // cap bytes
+  // class ballots: one warp: 2 x 64 slots in the xs area (a one-warp selection uses no
+  // cross-warp sums); cooperative: 8 warps x 2 x 16 slots after the lists
+  ss.bal = coop ? reinterpret_cast<uint32_t *>(base + 512 + D * 4 + cap * 9)
+                : reinterpret_cast<uint32_t *>(base);
+  ss.hist = ss.lj;   // 256 ints: the long-row selection does not use the list
+  return ss;
+}
+static_assert(512 + 128 * 4 + kAmbCapWarp * 9 <= kSelWarpBytes, "per-warp selection scratch");
+static_assert(2 * 64 * 4 <= 512, "per-warp class ballots in the xs area");
+static_assert(512 + 128 * 4 + kAmbCapCta * 9 + 8 * 2 * 16 * 4 <= kScratchBytes,
+              "cooperative selection scratch");
+static_assert((kAmbCapCta * 9) % 4 == 0, "aligned cooperative ballots");
+static_assert(kAmbCapWarp >= 256, "the radix histogram shares the list");
+
 template <int D, int NT>
 __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scratch,
                                FusedShared &sh KIN_TRACE_PARAM) {
   using C = Cfg<D, NT>;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = p.num_kv_heads;
+  const int H = p.num_kv_heads, G = p.group;
   const int b = d.row, h0 = d.x0, n = d.x1, hs = d.x2;
   const int nb = n + 1;
+  const int m = p.top_k - 1;
+  const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
   KIN_TIC(t_sw);
   if (tid == 0) {
     // Wait until every score item (chunk) of this (sequence, head range) has published.
     const int32_t *cnt = p.score_cnt + b * p.head_ranges + h0 / p.heads_per_range;
     const int expected = (n + p.score_chunk - 1) / p.score_chunk;
-    wait_flag(cnt, expected, sh, p.err);
+    sh.sel_ok = wait_flag(cnt, expected, sh, p.err) ? 1 : 0;
   }
   C::Bar::sync();
+  const bool ok = *reinterpret_cast<volatile int *>(&sh.sel_ok) != 0;
   KIN_TOC(kTrCSelWait, t_sw);
   if (d.first == 1) {   // one row, all consumer warps
     KIN_TIC(t_sel);
+    constexpr int NW = C::kCW;
     const int row = b * H + h0;
     const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
     int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
-    const int m = p.top_k - 1;
-    int *xs = reinterpret_cast<int *>(scratch);
-    constexpr int NW = C::kCW;
-    if (n <= NW * 32 * 2)
-      cta_select_row<2, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+    const SelScratch ss = sel_scratch<D>(scratch, kAmbCapCta, true);
+    const float E = __uint_as_float(__ldcg(p.bound + row));
+    const RefineCtx rc{p.cent_lo + h0 * D, trow, static_cast<int64_t>(H) * D, p.num_pages, ss.qs};
+    const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h0 * G) * D;
+    using Bar = typename C::Bar;
+    if (!ok)
+      fallback_kept(m, nb, out, tid, C::kCThreads);
+    else if (n <= NW * 32 * 2)
+      cta_select_row<2, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
     else if (n <= NW * 32 * 4)
-      cta_select_row<4, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+      cta_select_row<4, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
     else if (n <= NW * 32 * 8)
-      cta_select_row<8, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+      cta_select_row<8, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
     else if (n <= NW * 32 * 16)
-      cta_select_row<16, NW, typename C::Bar>(srow, n, m, nb, out, xs);
+      cta_select_row<16, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
     else if (warp == 0)   // longer rows: one warp, radix select over L2
-      warp_select(srow, n, m, nb, nullptr, reinterpret_cast<int *>(scratch) + 256, out, lane);
+      warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
     C::Bar::sync();
     if (tid == 0) st_release_gpu(p.ready + row, 1);
     KIN_TOC(kTrCSelComp, t_sel);
@@ -1235,21 +1676,26 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
     if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
     return;
   }
-  int *hist = reinterpret_cast<int *>(scratch) + warp * 256;   // longer rows only
+  const SelScratch ss = sel_scratch<D>(scratch + warp * kSelWarpBytes, kAmbCapWarp, false);
   KIN_TIC(t_sel);
   for (int hh = warp; hh < hs; hh += C::kCW) {
-    const int row = b * H + h0 + hh;
+    const int h = h0 + hh;
+    const int row = b * H + h;
     const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
     int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
-    const int m = p.top_k - 1;
-    if (n <= 32 * 16)
-      warp_select_bits<16>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
+    const float E = __uint_as_float(__ldcg(p.bound + row));
+    const RefineCtx rc{p.cent_lo + h * D, trow, static_cast<int64_t>(H) * D, p.num_pages, ss.qs};
+    const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h * G) * D;
+    if (!ok)
+      fallback_kept(m, nb, out, lane, 32);
+    else if (n <= 32 * 16)
+      warp_select_bits<16, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
     else if (n <= 32 * 32)
-      warp_select_bits<32>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
+      warp_select_bits<32, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
     else if (n <= 32 * 64)
-      warp_select_bits<64>(srow, n, m, nb, out, lane KIN_TRACE_ARG);
+      warp_select_bits<64, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
     else
-      warp_select(srow, n, m, nb, nullptr, hist, out, lane);
+      warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
     __syncwarp();
     if (lane == 0) st_release_gpu(p.ready + row, 1);
     __syncwarp();
@@ -1313,7 +1759,7 @@ __device__ void consume_attention(const FusedParams &p, const Desc &d, uint8_t *
         __syncwarp();
       } else if (append && i == cnt - 1) {
         // The final block just became complete: its centroid (fp32 sum over the 16
-        // tokens in order, times 1/16, rounded to bf16) from the staged keys.
+        // tokens in order, times 1/16) from the staged keys.
         constexpr int kPer = D / 32;
         float acc[kPer];
 #pragma unroll
@@ -1327,9 +1773,15 @@ __device__ void consume_attention(const FusedParams &p, const Desc &d, uint8_t *
             acc[k] = t == 0 ? x : __fadd_rn(acc[k], x);
           }
         }
-        __nv_bfloat16 *dst = p.cent_out + (static_cast<int64_t>(page) * H + h) * D + lane * kPer;
+        // both codes: the mean rounded to bf16, and its rounding residual rounded to bf16
+        const int64_t off = (static_cast<int64_t>(page) * H + h) * D + lane * kPer;
 #pragma unroll
-        for (int k = 0; k < kPer; ++k) dst[k] = __float2bfloat16_rn(__fmul_rn(acc[k], 1.0f / kBlock));
+        for (int k = 0; k < kPer; ++k) {
+          const float mean = __fmul_rn(acc[k], 1.0f / kBlock);
+          const __nv_bfloat16 c1 = __float2bfloat16_rn(mean);
+          p.cent_out[off + k] = c1;
+          p.cent_lo_out[off + k] = __float2bfloat16_rn(__fsub_rn(mean, __bfloat162float(c1)));
+        }
       }
       const uint32_t sK = smem_u32(stage);
       st.page(qb, sK, sK + Tile::kKBytes, ntok, scale_log2, lane);
@@ -1369,7 +1821,7 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
   while (true) {
     const int slot = nd % kDescs;
     KIN_TIC(t_d);
-    const bool got = wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err);
+    const bool got = wait_bar(&sh.dfull[slot], (nd / kDescs) & 1u, sh, p.err, true);
     KIN_TOC(kTrCDesc, t_d);
     if (!got) break;
     const Desc d = sh.desc[slot];

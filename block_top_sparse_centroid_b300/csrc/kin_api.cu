@@ -97,14 +97,14 @@ Plan make_plan(const kin_kv_cache *c, const kin_decode_args *a, int mode) {
 }
 
 // The counters of one decode call: the work-queue head, CTAs finished, score arrivals per
-// (sequence, head range), split arrivals and ready flags per row.  They sit at the start
+// (sequence, head range), split arrivals, ready flags and score error bounds per row.  They sit at the start
 // of the workspace, in an area of at least kCounterWords words that no other region
 // uses, and are zero between calls: a bf16 call whose counters fit in that area leaves
 // them zero itself (the last CTA of its kernel clears them), so it needs no clearing
 // launch; any other call clears its counters before its kernels and after them.
 constexpr size_t kCounterWords = 16384;
 struct Counters {
-  size_t work_next, exit_cnt, score_cnt, attn_cnt, ready, count;
+  size_t work_next, exit_cnt, score_cnt, attn_cnt, ready, bound, count;
 };
 Counters counter_layout(const kin_decode_args *a, const Plan &pl) {
   Counters k{};
@@ -113,7 +113,8 @@ Counters counter_layout(const kin_decode_args *a, const Plan &pl) {
   k.score_cnt = 2;
   k.attn_cnt = k.score_cnt + static_cast<size_t>(a->batch) * pl.head_ranges;
   k.ready = k.attn_cnt + pl.rows;
-  k.count = k.ready + pl.rows;
+  k.bound = k.ready + pl.rows;
+  k.count = k.bound + pl.rows;
   return k;
 }
 
@@ -257,23 +258,37 @@ kin_status encode_page_map(CUtensorMap *map, const kin_kv_cache *c, const void *
   return KIN_OK;
 }
 
-// Make the device that holds `ptr` current (the caller's framework may have another
-// device current in its own runtime instance).
-kin_status use_device_of(const void *ptr) {
-  cudaPointerAttributes attr;
-  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
-  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
-    return fail(KIN_ERR_INVALID_ARG, "cache pages are not device memory");
-  int cur = -1;
-  e = cudaGetDevice(&cur);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  if (cur != attr.device) {
-    e = cudaSetDevice(attr.device);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+// Makes the device that holds the cache current for the duration of one call (the
+// caller's framework may have another device current) and puts the caller's device back
+// when the call returns, on every path.
+class DeviceScope {
+ public:
+  DeviceScope() = default;
+  DeviceScope(const DeviceScope &) = delete;
+  DeviceScope &operator=(const DeviceScope &) = delete;
+  ~DeviceScope() {
+    if (prev_ >= 0) cudaSetDevice(prev_);
   }
-  return KIN_OK;
-}
+  kin_status enter(const void *ptr) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+      return fail(KIN_ERR_INVALID_ARG, "cache pages are not device memory");
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != attr.device) {
+      e = cudaSetDevice(attr.device);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+      prev_ = cur;
+    }
+    return KIN_OK;
+  }
+
+ private:
+  int prev_ = -1;   // the caller's device, when the call switched away from it
+};
 
 // Inside a stream capture the events become event-record nodes of the graph, so that a
 // replayed graph still timestamps its kernels.
@@ -303,7 +318,8 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
   if (events != nullptr && (events[0] == nullptr || events[1] == nullptr ||
                             events[2] == nullptr || events[3] == nullptr))
     return fail(KIN_ERR_INVALID_ARG, "events must hold 4 created CUDA events");
-  s = use_device_of(c->k_pages);
+  DeviceScope scope;
+  s = scope.enter(c->k_pages);
   if (s != KIN_OK) return s;
   uint8_t *ws = static_cast<uint8_t *>(a->workspace);
   int32_t *cnt = reinterpret_cast<int32_t *>(ws + L.counters);
@@ -332,8 +348,12 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     if (s != KIN_OK) return s;
     FusedParams fp{};
     fp.q = static_cast<const __nv_bfloat16 *>(a->q);
+    // the centroid table of a bf16 cache: plane 0 (first codes), then plane 1 (residuals)
+    const int64_t plane = c->num_pages * c->num_kv_heads * c->head_dim;
     fp.centroids = static_cast<const __nv_bfloat16 *>(a->centroids);
+    fp.cent_lo = fp.centroids == nullptr ? nullptr : fp.centroids + plane;
     fp.cent_out = static_cast<__nv_bfloat16 *>(a->centroids);
+    fp.cent_lo_out = fp.cent_out == nullptr ? nullptr : fp.cent_out + plane;
     fp.block_table = a->block_table;
     fp.seq_lens = a->seq_lens;
     fp.out = a->out;
@@ -346,6 +366,7 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.score_cnt = cnt + ck.score_cnt;
     fp.attn_cnt = cnt + ck.attn_cnt;
     fp.ready = cnt + ck.ready;
+    fp.bound = reinterpret_cast<uint32_t *>(cnt + ck.bound);
     fp.exit_cnt = cnt + ck.exit_cnt;
     fp.counters = cnt;
     fp.n_counters = static_cast<int>(ck.count);
@@ -480,7 +501,8 @@ kin_status run_centroids(const kin_kv_cache *c, const int32_t *page_ids, int64_t
     return fail(KIN_ERR_INVALID_ARG, "page_ids is NULL but n (%lld) != num_pages (%lld)",
                 (long long)n, (long long)c->num_pages);
   if (n == 0) return ok();
-  s = use_device_of(c->k_pages);
+  DeviceScope scope;
+  s = scope.enter(c->k_pages);
   if (s != KIN_OK) return s;
   cudaError_t e = launch_centroids(c->dtype, c->head_dim, c->num_kv_heads, c->k_pages,
                                    c->num_pages, page_ids, n, centroids, err, stream);

@@ -14,8 +14,13 @@ constexpr int kBlock = 16;                 // tokens per block == tokens per KV 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Bounded waits: a try_wait suspends the thread for a hardware-chosen time slice, so
-// this many attempts is far beyond any legitimate copy latency (seconds), yet ends.
-constexpr uint32_t kMaxWaitTries = 1u << 22;
+// this many attempts is far beyond any legitimate copy latency (seconds), yet ends.  A
+// build may set a smaller limit (-DKIN_MAX_WAIT_TRIES=n) to make a wait that can never
+// complete give up quickly.
+#ifndef KIN_MAX_WAIT_TRIES
+#define KIN_MAX_WAIT_TRIES (1u << 22)
+#endif
+constexpr uint32_t kMaxWaitTries = KIN_MAX_WAIT_TRIES;
 
 __device__ __forceinline__ void flag_error(int32_t *flag, int bits) {
   if (flag != nullptr) atomicOr(flag, bits);

@@ -64,8 +64,10 @@ cudaError_t launch_attention_f32(int head_dim, const AttnParams &p, cudaStream_t
 //   attention     (row = b * H + h, split): attention over one split of the kept list
 struct FusedParams {
   const __nv_bfloat16 *q;          // [B, H*G, d]
-  const __nv_bfloat16 *centroids;  // [P, H, d]
-  __nv_bfloat16 *cent_out;         // centroid table written when append_final is set
+  const __nv_bfloat16 *centroids;  // [P, H, d] first centroid code (the fp32 mean in bf16)
+  const __nv_bfloat16 *cent_lo;    // [P, H, d] second code (the rounding residual in bf16)
+  __nv_bfloat16 *cent_out;         // both planes written when append_final is set
+  __nv_bfloat16 *cent_lo_out;
   const int32_t *block_table;      // [B, max_blocks]
   const int32_t *seq_lens;         // [B]
   void *out;                       // [B, H*G, d]
@@ -78,6 +80,7 @@ struct FusedParams {
   int32_t *score_cnt;              // [B * head_ranges] finished score items
   int32_t *attn_cnt;               // [B*H] split arrivals
   int32_t *ready;                  // [B*H] selection published
+  uint32_t *bound;                 // [B*H] score error bound of the row (fp32 bits, max)
   int32_t *exit_cnt;               // CTAs finished (self_clean only)
   int32_t *counters;               // all of the above counters, n_counters words
   int n_counters;

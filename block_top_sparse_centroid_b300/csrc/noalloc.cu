@@ -48,8 +48,19 @@ extern "C" kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
     return set_error(KIN_ERR_UNSUPPORTED, "device %d is beyond the %d supported", dev, kMaxDevices);
   int cur = -1;
   e = cudaGetDevice(&cur);
-  if (e == cudaSuccess && cur != dev) e = cudaSetDevice(dev);
-  if (e != cudaSuccess) return set_error(KIN_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return set_error(KIN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (cur != dev) {
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return set_error(KIN_ERR_CUDA, "cudaSetDevice: %s", cudaGetErrorString(e));
+  }
+  // the caller's device is current again when this call returns, on every path
+  struct Restore {
+    int prev;
+    bool switched;
+    ~Restore() {
+      if (switched) cudaSetDevice(prev);
+    }
+  } restore{cur, cur != dev};
   void *scratch = nullptr;
   {
     // First call on a device: resolve the array's device address with that device

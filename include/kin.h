@@ -28,6 +28,9 @@
  *     the given stream (a cudaStream_t; NULL = the legacy default stream) and runs
  *     asynchronously.  The caller owns every buffer and keeps it alive until the
  *     stream reaches the enqueued work.
+ *   - Every call runs on the device that holds the cache's pages (it makes that device
+ *     current while it enqueues) and leaves the calling thread's current device as it
+ *     found it, on every return path.
  *   - Arguments are validated on the host before anything is enqueued; a bad argument
  *     returns a status and enqueues nothing.  kin_last_error() gives a one-line reason.
  *   - Errors only the device can see (a block-table entry outside [0, num_pages), a
@@ -97,15 +100,18 @@ typedef struct {
   const void *q;          /* [B, H*G, d]                                              */
   const int32_t *block_table; /* [B, max_blocks] physical page of logical block j      */
   const int32_t *seq_lens;    /* [B] tokens incl. the current one; nb = ceil(L/16)     */
-  void *centroids;        /* [P, H, d] block centroids (kin_centroids_build): read by block
-                             top-k; rows of complete final blocks written when flags has
-                             KIN_DECODE_APPEND_FINAL; unused by dense otherwise          */
+  void *centroids;        /* block centroids (kin_centroids_build): fp32 caches [P, H, d];
+                             bf16 caches [2, P, H, d] (plane 0: the fp32 mean rounded to
+                             bf16, plane 1: its rounding residual rounded to bf16).  Read
+                             by block top-k; rows of complete final blocks written when
+                             flags has KIN_DECODE_APPEND_FINAL; unused by dense otherwise */
   void *out;              /* [B, H*G, d] attention output                              */
   float *lse;             /* optional [B, H*G]: natural-log sum of exp(sm_scale * q.k)  */
   int32_t *sel_blocks;    /* optional [B, H, top_k]: kept logical blocks, ascending,
                              -1 padded when nb < k (block top-k only)                   */
   float *scores;          /* optional [B, H, max_blocks]: group scores of blocks
-                             0..nb-2 of rows with nb > k (other entries untouched)      */
+                             0..nb-2 of rows with nb > k (other entries untouched); for
+                             bf16 caches computed from plane 0 of the centroids          */
   void *workspace;        /* scratch of kin_workspace_size() bytes, 256-byte aligned.
                              Zero-fill it once before its first use (cudaMemset); after
                              that only decode calls may write it: every call leaves its
@@ -138,13 +144,19 @@ KIN_API kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decod
                               int32_t mode, size_t *bytes);
 
 /* Centroid (mean key) of every listed page, for every KV head:
- *   centroids[p, h, :] = (sum_{t<16} K[p, h, t, :]) / 16
- * summed in fp32 in ascending t, stored in cache->dtype (bf16: round-to-nearest-even).
- * Blocks are ranked by this mean key -- Pith review, "What carries the argument".
+ *   c[p, h, :] = (sum_{t<16} K[p, h, t, :]) / 16
+ * summed in fp32 in ascending t.  Blocks are ranked by this mean key -- Pith review,
+ * "What carries the argument".  fp32 caches store c in centroids[p, h, :].  bf16 caches
+ * store two bf16 codes per element: centroids[0, p, h, :] = bf16(c) (round-to-nearest-
+ * even) and centroids[1, p, h, :] = bf16(c - bf16(c)) (the difference is exact in fp32),
+ * whose sum is c to about 2^-16 of its size.  Block scores are streamed from plane 0;
+ * plane 1 settles the candidates whose plane-0 scores lie too close to the cut to rank
+ * them as the fp32 mean would.
  * page_ids: device int32[n] physical page ids (pages must hold 16 valid tokens), or
  * NULL for all pages 0..num_pages-1 (then n must equal num_pages).  centroids: device
- * [num_pages, H, d]; only the listed pages' rows are written.  Ids outside
- * [0, num_pages) are skipped and flagged in *err_flag (optional). */
+ * [num_pages, H, d] (fp32) or [2, num_pages, H, d] (bf16); only the listed pages' rows
+ * are written.  Ids outside [0, num_pages) are skipped and flagged in *err_flag
+ * (optional). */
 KIN_API kin_status kin_centroids_build(const kin_kv_cache *cache, const int32_t *page_ids, int64_t n,
                                void *centroids, int32_t *err_flag, kin_stream_t stream);
 
@@ -155,12 +167,19 @@ KIN_API kin_status kin_centroids_append(const kin_kv_cache *cache, const int32_t
 
 /* One block top-k decode step: for every sequence b and KV head h with
  * nb = ceil(seq_lens[b] / 16) blocks:
- *   score   s_j = sum_g q[b, hG+g, :] . centroids[block_table[b, j], h, :],  j < nb-1
+ *   score   s_j = sum_g q[b, hG+g, :] . c[block_table[b, j], h, :],  j < nb-1
  *   select  S = {nb-1} + the k-1 largest s_j (ties to lower j); all blocks if nb <= k
  *   attend  out[b, hG+g, :] = softmax over the valid tokens of S of sm_scale * q.k, applied to V
- * Pith review, "What carries the argument"; Kinetics README, "Benchmark Block TopK
- * Attention throughput".  Needs args->centroids built for every complete block that
- * can be scored (all blocks but the final one of each sequence). */
+ * with c the fp32 block mean.  Pith review, "What carries the argument"; Kinetics README,
+ * "Benchmark Block TopK Attention throughput".  Needs args->centroids built for every
+ * complete block that can be scored (all blocks but the final one of each sequence).
+ * bf16 caches: every candidate is scored with plane 0 of the centroids (fp32
+ * arithmetic); with E a bound on that score's distance from the fp32-mean score over the
+ * row, candidates more than 2E above (below) the k-th score are kept (dropped), and
+ * those in between are re-scored with both planes before the cut is made.  The kept set
+ * is therefore the fp32-mean ranking's, up to rankings that the two planes cannot
+ * separate (score differences of about 2^-16 of the scores' size).  args->scores holds
+ * the plane-0 scores.  Outputs are undefined when the call sets KIN_DEVERR_TIMEOUT. */
 KIN_API kin_status kin_blocktopk_decode(const kin_kv_cache *cache, const kin_decode_args *args,
                                 kin_stream_t stream);
 

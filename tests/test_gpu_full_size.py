@@ -4,10 +4,11 @@ top-k decode call with the fused centroid append of the pages the current token 
 
 Rows of full-size workloads are too many for the oracle to check all of them, so:
 * every row: the kept list is valid (ascending, distinct, min(nb, k) blocks, the final
-  block last) and every output and lse is finite;
+  block last) and admissible against the oracle's fp32-centroid selection (bit-exact, or
+  differing only inside the 1e-3 near-tie band); every output and lse is finite;
 * a seeded sample of rows (plus the first and the last row): selection, scores, outputs
   and lse against the oracle, one row at a time, with the tolerances of the small-size
-  tests;
+  tests (near-tie rows against the oracle's attention over the admissible set kept);
 * every appended centroid: bit-exact against the oracle's centroid of that page;
 * dense decode (the comparison baseline) on a few sampled rows.
 """
@@ -20,7 +21,8 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 if torch.cuda.is_available():
-    from _gpu import DeviceState, check_centroids, compare_rows  # noqa: E402
+    from _gpu import (DeviceState, check_centroids, compare_rows,  # noqa: E402
+                      oracle_centroid_table, selection_report)
 
 SAMPLED_ROWS = 12
 
@@ -57,11 +59,16 @@ def test_full_size_workload(name):
     assert np.isfinite(res["out"]).all()
     assert np.isfinite(res["lse"]).all()
 
+    rep = selection_report(inp, res["sel"], oracle_centroid_table(inp))
+    print(f"{name}: {rep['rows']} rows, {rep['outside']} outside the near-tie band, "
+          f"{rep['near_tie']} near ties, {rep['bf16_rank_diff']} differ from the bf16-centroid "
+          f"ranking")
+    assert rep["outside"] == 0, rep
+
     rows = W.sample_rows(cfg, SAMPLED_ROWS, seed=FULL_SIZE[name])
     rows = sorted(set(rows) | {(0, 0), (cfg.batch - 1, cfg.num_kv_heads - 1)})
     stats = compare_rows(inp, res, rows)
-    assert stats["rows"] + stats["near_tie_rows"] == len(rows)
-    assert stats["rows"] >= len(rows) - 2, stats
+    assert stats["rows"] == len(rows)
 
     if st.just_pages:
         check_centroids(inp, st.cents, st.just_pages)

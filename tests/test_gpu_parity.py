@@ -114,7 +114,7 @@ def test_unshuffled_and_shared_pages():
     # best-of-N layout: every sample shares the prompt's pages
     cfg = W.find_config("best-of-n-qwen3-14b").scaled(batch=6, ctx_lo=300, ctx_hi=900, prefix=256, steps=1)
     inp, st, res, stats = _run(cfg)
-    assert stats["rows"] + stats["near_tie_rows"] == cfg.batch * cfg.num_kv_heads
+    assert stats["rows"] == cfg.batch * cfg.num_kv_heads
 
 
 def test_duplicate_blocks_tie_to_lower_index():
@@ -237,7 +237,8 @@ def test_decode_appends_completed_final_blocks(dtype, d, dense):
     inp = W.generate(cfg)
     st = DeviceState(inp, append=False)         # final pages' centroids not built yet
     assert st.just_pages
-    zero = st.cents[torch.tensor(st.just_pages, device=st.dev).long()]
+    idx = torch.tensor(st.just_pages, device=st.dev).long()
+    zero = st.cents[:, idx] if dtype == "bf16" else st.cents[idx]   # bf16: both planes
     assert int(zero.float().abs().sum()) == 0
     res = st.decode(dense=dense, append_final=True)
     torch.cuda.synchronize()

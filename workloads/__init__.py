@@ -21,9 +21,11 @@ to 32K tokens.  The value recipe is:
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import hashlib
 import math
+import os
 from typing import List, Optional
 
 import torch
@@ -160,11 +162,15 @@ def _draw_lengths(cfg: Config) -> torch.Tensor:
 
 def _fill_pages(num_pages: int, cfg: Config, purpose: str, with_offset: bool,
                 chunk: int = 1024):
-    """Draw [num_pages, H, 16, d] values chunk by chunk (fp32), plus the K offsets."""
+    """Draw [num_pages, H, 16, d] values chunk by chunk (fp32), plus the K offsets.
+
+    Every chunk has its own generator (seeded from its first page), so the chunks are
+    drawn on several threads with the same values as one after the other."""
     H, d = cfg.num_kv_heads, cfg.head_dim
     out = torch.empty((num_pages, H, BLOCK, d), dtype=torch_dtype(cfg.dtype))
     offs = torch.zeros((num_pages, H, d), dtype=torch.float32) if with_offset else None
-    for c0 in range(0, num_pages, chunk):
+
+    def fill(c0):
         c1 = min(num_pages, c0 + chunk)
         g = _gen(cfg.seed, purpose, c0)
         x = torch.randn((c1 - c0, H, BLOCK, d), generator=g, dtype=torch.float32)
@@ -173,6 +179,15 @@ def _fill_pages(num_pages: int, cfg: Config, purpose: str, with_offset: bool,
             offs[c0:c1] = o
             x += o[:, :, None, :]
         out[c0:c1] = x.to(out.dtype)
+
+    starts = list(range(0, num_pages, chunk))
+    workers = min(len(starts), os.cpu_count() or 1, 32)
+    if workers <= 1:
+        for c0 in starts:
+            fill(c0)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+            list(ex.map(fill, starts))
     return out, offs
 
 
@@ -243,11 +258,14 @@ def mark_stale_slots(inp: Inputs) -> None:
 
 @dataclasses.dataclass
 class StepTokens:
-    """One decode step of the best-of-N workload: the new token's q, k and v per sample."""
+    """One decode step of the best-of-N workload: the new token's q, k and v per sample,
+    and where its k and v go (position L_b of each sequence before the step)."""
 
     q: torch.Tensor        # [batch, num_q_heads, head_dim]
     k_new: torch.Tensor    # [batch, num_kv_heads, head_dim]
     v_new: torch.Tensor    # [batch, num_kv_heads, head_dim]
+    pages: torch.Tensor    # [batch] int64 physical page of position L_b
+    slots: torch.Tensor    # [batch] int64 slot of position L_b in that page
 
 
 def step_tokens(inp: Inputs, step: int) -> StepTokens:
@@ -262,7 +280,7 @@ def step_tokens(inp: Inputs, step: int) -> StepTokens:
     pages = inp.block_table[torch.arange(B), L // BLOCK].to(torch.int64)
     k += inp.k_offset[pages]
     dt = torch_dtype(cfg.dtype)
-    return StepTokens(q.to(dt), k.to(dt), v.to(dt))
+    return StepTokens(q.to(dt), k.to(dt), v.to(dt), pages, L % BLOCK)
 
 
 def write_step_tokens(inp: Inputs, tok: StepTokens) -> torch.Tensor:
@@ -271,16 +289,29 @@ def write_step_tokens(inp: Inputs, tok: StepTokens) -> torch.Tensor:
     Writes k_new / v_new at position L_b, advances seq_lens, replaces q, and returns the
     physical ids of the pages that this write completed (16 valid tokens now).
     """
-    B = inp.cfg.batch
-    L = inp.seq_lens.to(torch.int64)
-    pages = inp.block_table[torch.arange(B), L // BLOCK].to(torch.int64)
-    slots = L % BLOCK
+    pages, slots = tok.pages, tok.slots
     inp.k_pages[pages, :, slots, :] = tok.k_new
     inp.v_pages[pages, :, slots, :] = tok.v_new
     inp.seq_lens += 1
     inp.q = tok.q
     done = (slots == BLOCK - 1)
     return pages[done].to(torch.int32)
+
+
+def decode_plan(inp: Inputs) -> List[Optional[StepTokens]]:
+    """The tokens of the workload's decode steps 0 .. steps-1, advancing the host state.
+
+    Step 0 decodes the initial state (its current token is already in the cache: entry
+    None); step t >= 1 first appends the token it draws at position L_b of every sequence.
+    The host cache ends in the state of the last step.  Pages were allocated for every
+    step's token by ``generate``.
+    """
+    plan: List[Optional[StepTokens]] = [None]
+    for t in range(1, inp.cfg.steps):
+        tok = step_tokens(inp, t)
+        write_step_tokens(inp, tok)
+        plan.append(tok)
+    return plan
 
 
 def qwen3_sizes(cfg: Config) -> dict:
@@ -334,5 +365,5 @@ def find_config(name_or_index) -> Config:
 
 
 __all__ = ["BLOCK", "POISON_K", "POISON_V", "Config", "CONFIGS", "Inputs", "StepTokens",
-           "generate", "step_tokens", "write_step_tokens", "mark_stale_slots",
+           "generate", "step_tokens", "write_step_tokens", "decode_plan", "mark_stale_slots",
            "sample_rows", "find_config", "host_arrays", "row_problem", "torch_dtype", "qwen3_sizes"]
