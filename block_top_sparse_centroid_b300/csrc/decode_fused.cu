@@ -65,6 +65,8 @@ constexpr int kDescs = 8;                           // descriptor slots producer
 constexpr int kMaxScoreChunk = 256;                 // candidate blocks per score item
 constexpr int kHeadsPerRange = 32;                  // KV heads per score / select item
 constexpr int kScoreSlots = 16;                     // score-item arrival counters (> kDescs)
+constexpr int kRefineRows = 8;                      // rows per refine item (one warp each)
+constexpr int kRefinePerStage = 28;                 // ambiguous candidates per refine ring stage
 // Consumer scratch: the combine buffers of an attention item, the group-summed queries
 // of a score item, or the histograms of the selections (never at once).
 constexpr int kScratchBytes = 34 * 1024;
@@ -107,6 +109,10 @@ struct Ring {
   __device__ static __forceinline__ uint32_t phase(uint32_t n) { return (n / kPer) & 1u; }
 };
 
+static_assert(256 + kRefinePerStage * 128 * 2 <= BfTile<128>::kStageBytes, "refine stage, d = 128");
+static_assert(256 + kRefinePerStage * 64 * 2 <= BfTile<64>::kStageBytes, "refine stage, d = 64");
+static_assert(kRefinePerStage * 8 <= 256, "refine stage header");
+
 // Score items of up to 8 heads and groups of up to 8 query heads (NT = 1) get their raw q
 // rows staged by a bulk copy into one of two slots, so that no consumer waits on a global
 // load of q (a dependent load costs microseconds while HBM is saturated).
@@ -120,7 +126,8 @@ constexpr size_t fused_smem_bytes() {
   return 1024 + Ring<D, NT>::kBytes + kScratchBytes + q_stage_bytes<NT>();
 }
 
-enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4 };
+enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4,
+             kDescRefine = 5 };
 enum : int { kAttnEveryBlock = 1, kAttnAppendLast = 2 };
 
 // A work item as the producer hands it to the consumers.
@@ -197,6 +204,21 @@ __device__ __forceinline__ bool wait_flag(const int32_t *flag, int target, Fused
   *reinterpret_cast<volatile int *>(&sh.abort) = 1;
   flag_error(err, KIN_DEVERR_TIMEOUT);
   return false;
+}
+
+// wait_flag returning the value seen (the last one read when the wait gives up).
+__device__ __forceinline__ int wait_flag_value(const int32_t *flag, int target, FusedShared &sh,
+                                               int32_t *err) {
+  int v = 0;
+  for (uint32_t i = 0; i < kMaxWaitTries; ++i) {
+    v = ld_acquire_gpu(flag);
+    if (v >= target) return v;
+    if ((i & 255u) == 255u && *reinterpret_cast<volatile int *>(&sh.abort) != 0) return v;
+    __nanosleep(64);
+  }
+  *reinterpret_cast<volatile int *>(&sh.abort) = 1;
+  flag_error(err, KIN_DEVERR_TIMEOUT);
+  return v;
 }
 
 // Bounded wait until the shared counter *cnt >= target.  Same abort rule as wait_bar.
@@ -278,10 +300,12 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // ----------------------------------------------------------------------------------
 // Selection.  The kernel scores every candidate with the first centroid code (bf16), which
 // is what it can stream at full bandwidth; the reference ranking is by the fp32 mean.  With
-// E >= |s - s*| for every candidate of the row (p.bound) and T the m-th largest score s, a
-// candidate with s > T + 2E is in the top m by s* as well (only candidates with s > T, at
-// most m - 1 of them, can beat it), and one with s < T - 2E is out (every candidate with
-// s >= T, at least m of them, beats it).  The candidates in between ("ambiguous") are
+// E >= |s - s*| for every candidate of the row (p.bound) and a threshold T that at most m
+// scores exceed and at least m reach (the m-th largest score, or a smaller value at which
+// exactly m scores are >= T, where the search stops early), a candidate with s > T + 2E is
+// in the top m by s* as well (only candidates with s > T, at most m of them counting
+// itself, can beat it), and one with s < T - 2E is out (every candidate with s >= T, at
+// least m of them, beats it).  The candidates in between ("ambiguous") are
 // re-scored with both codes, s + qs . c2, which is the score of the fp32 mean to about
 // 2^-16 of its size, and the m - (number in) best of them are kept, equal scores to the
 // lower block index.  The selection runs on modified keys: in -> kKeyIn, out -> 0,
@@ -289,9 +313,8 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // the kept list.  Keys of real scores are >= 2, padding slots 0.
 // ----------------------------------------------------------------------------------
 constexpr uint32_t kKeyIn = 0xffffffffu;   // above the key of every number (+inf: 0xff800000)
-// Ambiguous candidates a selecting warp (a cooperative CTA) lists and re-scores at once.
+// Ambiguous candidates a row's selection can list for its refine item.
 constexpr int kAmbCapWarp = 256;
-constexpr int kAmbCapCta = 1024;
 
 struct Window {
   uint32_t lo, hi;   // in: key > hi; ambiguous: lo <= key <= hi; out: key < lo
@@ -370,21 +393,6 @@ __device__ __forceinline__ void group_query(const __nv_bfloat16 *qg, int G, floa
   }
 #pragma unroll
   for (int i = 0; i < kPer; ++i) qs[lane * kPer + i] = acc[i];
-}
-
-// Re-score the n_amb listed ambiguous candidates (lj) into lr by the NTHR threads
-// ti = 0 .. NTHR - 1, one candidate per thread at a time: its first-code score is read back
-// from the row's scores alongside its page.  In a one-warp selection the caller's key
-// registers are dead by then (only the class ballots are needed afterwards), which leaves
-// room for a row's loads in flight.
-template <int D, int NTHR>
-__device__ __forceinline__ void refine_listed(const RefineCtx &rc, const float *srow, const int *lj,
-                                              uint32_t *lr, int n_amb, int ti, int lane) {
-  for (int e = ti; e < n_amb; e += NTHR) {
-    const int j = lj[e];
-    const float s = __ldcg(srow + j);
-    lr[e] = refined_key<D, 1>(rc, j, s, lane);
-  }
 }
 
 // m-th largest of the keys held in registers by one warp (lane l: slots i, candidate
@@ -489,18 +497,52 @@ __device__ __forceinline__ void classify(const uint32_t (&key)[KPL], const Windo
   __syncwarp();
 }
 
-// List the ambiguous candidates of slots 0 .. nslots - 1 with rank (in index order over the
-// whole row) in [0, cap) into lj.  Ranks of this warp start at rank0; slot i, lane l holds
-// candidate jbase + l + 32 i.
-__device__ __forceinline__ void list_amb(const uint32_t *bal, int nslots, int rank0, int cap,
-                                         int jbase, int *lj, int lane) {
+// classify for one warp that also writes, in the same pass, the certain candidates to
+// out[0 .. n_in) (ascending) and the ambiguous ones with their first-code scores to
+// lst[0 .. min(n_amb, cap)) (ascending).
+template <int KPL>
+__device__ __forceinline__ void classify_emit(const uint32_t (&key)[KPL], const Window &w,
+                                              uint32_t *bal, int32_t *out, int2 *lst, int cap,
+                                              int &n_in, int &n_amb, int lane) {
   const unsigned lt = (1u << lane) - 1u;
-  int base = rank0;
-  for (int i = 0; i < nslots; ++i) {
-    const unsigned ba = bal[nslots + i];
-    const int rank = base + __popc(ba & lt);
-    if (((ba >> lane) & 1u) && rank < cap) lj[rank] = jbase + lane + 32 * i;
-    base += __popc(ba);
+  int a = 0, b = 0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const bool is_in = key[i] > w.hi, is_amb = key[i] >= w.lo && key[i] <= w.hi;
+    const unsigned bi = __ballot_sync(0xffffffffu, is_in);
+    const unsigned ba = __ballot_sync(0xffffffffu, is_amb);
+    if (lane == 0) {
+      bal[i] = bi;
+      bal[KPL + i] = ba;
+    }
+    if (is_in) out[a + __popc(bi & lt)] = lane + 32 * i;
+    const int rank = b + __popc(ba & lt);
+    if (is_amb && rank < cap) lst[rank] = make_int2(lane + 32 * i, __float_as_int(key_score(key[i])));
+    a += __popc(bi);
+    b += __popc(ba);
+  }
+  n_in = a;
+  n_amb = b;
+  __syncwarp();
+}
+
+// The same writes for the warps of a cooperative selection, from their class ballots:
+// this warp's certain candidates go to out[in0 ..], its ambiguous ones to lst[amb0 ..].
+template <int KPL>
+__device__ __forceinline__ void emit_in_and_list(const uint32_t (&key)[KPL], const uint32_t *bal,
+                                                 int in0, int amb0, int jbase, int32_t *out,
+                                                 int2 *lst, int cap, int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int a = in0, b = amb0;
+#pragma unroll
+  for (int i = 0; i < KPL; ++i) {
+    const unsigned bi = bal[i], ba = bal[KPL + i];
+    const int j = jbase + lane + 32 * i;
+    if ((bi >> lane) & 1u) out[a + __popc(bi & lt)] = j;
+    const int rank = b + __popc(ba & lt);
+    if (((ba >> lane) & 1u) && rank < cap) lst[rank] = make_int2(j, __float_as_int(key_score(key[i])));
+    a += __popc(bi);
+    b += __popc(ba);
   }
 }
 
@@ -534,19 +576,22 @@ __device__ __forceinline__ void choose_amb(const uint32_t *lr, int na, int r, ui
   }
 }
 
-// Index-order compaction from the class ballots (classify): a candidate is kept when it
-// is in, or ambiguous and chosen (lf[rank] != 0; lf == NULL: every ambiguous one).  Ranks
-// of this warp's ambiguous candidates start at rank0; its kept candidates go to out[pos0 ..].
-__device__ __forceinline__ void emit_kept(const uint32_t *bal, int nslots, const uint8_t *lf,
-                                          int rank0, int pos0, int m, int jbase, int32_t *out,
-                                          int lane) {
+// Index-order compaction from the class ballots (classify): the in candidates (take_in),
+// and the ambiguous ones that are chosen (take_amb; lf[rank] != 0, or when lf is NULL the
+// first amb_limit of them in index order).  Ranks of this warp's ambiguous candidates start at rank0; its emitted candidates
+// go to out[pos0 ..] (at most up to out[m - 1]).
+__device__ __forceinline__ void emit_class(const uint32_t *bal, int nslots, const uint8_t *lf,
+                                           bool take_in, bool take_amb, int rank0, int pos0,
+                                           int m, int jbase, int32_t *out, int lane,
+                                           int amb_limit = 0x7fffffff) {
   const unsigned lt = (1u << lane) - 1u;
   int base = rank0, written = pos0;
   for (int i = 0; i < nslots; ++i) {
     const unsigned bi = bal[i], ba = bal[nslots + i];
     const bool a = ((ba >> lane) & 1u) != 0;
     const int rank = base + __popc(ba & lt);
-    const bool keep = ((bi >> lane) & 1u) != 0 || (a && (lf == nullptr || lf[rank] != 0));
+    const bool keep = (take_in && ((bi >> lane) & 1u) != 0) ||
+                      (take_amb && a && (lf == nullptr ? rank < amb_limit : lf[rank] != 0));
     const unsigned km = __ballot_sync(0xffffffffu, keep);
     const int pos = written + __popc(km & lt);
     if (keep && pos < m) out[pos] = jbase + lane + 32 * i;
@@ -555,27 +600,18 @@ __device__ __forceinline__ void emit_kept(const uint32_t *bal, int nslots, const
   }
 }
 
-// This warp's kept count under the class ballots and flags (see emit_kept).
-__device__ __forceinline__ int kept_count(const uint32_t *bal, int nslots, const uint8_t *lf,
-                                          int rank0, int lane) {
-  const unsigned lt = (1u << lane) - 1u;
-  int base = rank0, c = 0;
-  for (int i = 0; i < nslots; ++i) {
-    const unsigned bi = bal[i], ba = bal[nslots + i];
-    const bool keep = ((bi >> lane) & 1u) != 0 ||
-                      (((ba >> lane) & 1u) != 0 && lf[base + __popc(ba & lt)] != 0);
-    c += __popc(__ballot_sync(0xffffffffu, keep));
-    base += __popc(ba);
-  }
-  return c;
-}
+// Kept lists are released in two phases (the row's ready word): first the candidates that
+// are in for certain (positions 0 .. n_in - 1, ascending) and the final block (position m),
+// ready word n_in + 1, by the selection; then the chosen ambiguous ones (positions
+// n_in .. m - 1, ascending), ready word kReadyAll, by the row's refine item.  The attention
+// streams the first part meanwhile.  A selection that settles its row itself (no
+// ambiguous candidate to re-score) releases kReadyAll at once.  The caller's copy
+// (sel_out) is ascending.
+constexpr int kReadyAll = 1 << 30;
 
 // Scratch of one selecting warp (or of the CTA in a cooperative selection).
 struct SelScratch {
-  float *qs;      // [D]
-  int *lj;        // [cap] listed ambiguous candidates
-  uint32_t *lr;   // [cap] their re-scored keys
-  uint8_t *lf;    // [cap] 1 = kept
+  float *qs;      // [D] group-summed query (rows too long for the registers)
   uint32_t *bal;  // [2 * slots] class ballots of the warp (cooperative: per warp)
   int *hist;      // [256] radix histograms (rows too long for the registers)
   int *xs;        // [128] cross-warp partial sums (cooperative selection)
@@ -587,14 +623,15 @@ __device__ void warp_select_long(const float *srow, int n, int m, int nb, float 
                                  const SelScratch &ss, int32_t *out, int lane);
 
 // Kept blocks of one row by one warp, keys in registers: lane l holds candidates
-// j = l + 32 i, i < KPL (n <= 32 KPL).  out[0..m) = the m kept candidates ascending,
-// out[m] = nb - 1.  After the window classifies the candidates, only the class masks and
-// the listed ambiguous candidates are needed: the registers of the keys are free for the
-// re-scoring loads.
+// j = l + 32 i, i < KPL (n <= 32 KPL).  Writes the kept list out[0 .. m] (the final block
+// nb - 1 at out[m]) and returns true when the row is settled; returns false after the
+// first release phase, leaving the ambiguous candidates (lst, meta) to the row's refine
+// item.
 template <int KPL, int D>
-__device__ void warp_select_bits(const float *srow, int n, int m, int nb, float E,
+__device__ bool warp_select_bits(const float *srow, int n, int m, int nb, float E,
                                  const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
-                                 const SelScratch &ss, int32_t *out, int lane KIN_TRACE_PARAM) {
+                                 const SelScratch &ss, int32_t *out, int32_t *out_user,
+                                 int32_t *ready, int2 *lst, int2 *meta, int lane KIN_TRACE_PARAM) {
   KIN_TIC(t_k);
   uint32_t key[KPL];
   const int nv = n > lane ? (n - lane + 31) / 32 : 0;   // this lane's candidates
@@ -602,46 +639,44 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, float 
     float sv[KPL];   // every load issued before any is used
 #pragma unroll
     for (int i = 0; i < KPL; ++i) sv[i] = i < nv ? __ldcg(srow + lane + 32 * i) : 0.f;
-    // the group-summed query for a re-scoring, while the scores are in flight
-    group_query<D>(qg, G, const_cast<float *>(rc.qs), lane);
 #pragma unroll
     for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 2u) : 0u;
   }
   KIN_TOC(kTrCSelKeys, t_k);
-  if (m > 0) {
-    KIN_TIC(t_p);
-    bool exact;
-    const uint32_t t = bits_threshold<KPL>(key, m, exact);
-    const Window w = make_window(t, E);
-    int n_in, n_amb;
-    classify<KPL>(key, w, ss.bal, n_in, n_amb, lane);
-    const int r = m - n_in;
-    if (n_amb == r) {              // every ambiguous candidate is kept: no re-scoring
-      emit_kept(ss.bal, KPL, nullptr, 0, 0, m, 0, out, lane);
-    } else if (n_amb > kAmbCapWarp) {
-      // more ambiguous candidates than the list holds (clustered scores): the exact
-      // selection that re-reads the row instead of holding it
-      warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
-      return;
-    } else {
-      list_amb(ss.bal, KPL, 0, kAmbCapWarp, 0, ss.lj, lane);
-      __syncwarp();
-      if (w.refine) {
-        refine_listed<D, 32>(rc, srow, ss.lj, ss.lr, n_amb, lane, lane);
-      } else {
-        for (int e = lane; e < n_amb; e += 32) ss.lr[e] = 2u;
-      }
-      __syncwarp();
-      if (n_amb <= 32 * 2)
-        choose_amb<2>(ss.lr, n_amb, r, ss.lf, lane);
-      else
-        choose_amb<kAmbCapWarp / 32>(ss.lr, n_amb, r, ss.lf, lane);
-      __syncwarp();
-      emit_kept(ss.bal, KPL, ss.lf, 0, 0, m, 0, out, lane);
-    }
-    KIN_TOC(kTrCSelPass, t_p);
+  if (lane == 0) {
+    out[m] = nb - 1;
+    if (out_user != nullptr) out_user[m] = nb - 1;
   }
-  if (lane == 0) out[m] = nb - 1;
+  if (m == 0) return true;
+  KIN_TIC(t_p);
+  bool exact;
+  const uint32_t t = bits_threshold<KPL>(key, m, exact);
+  const Window w = make_window(t, E);
+  int n_in, n_amb;
+  classify_emit<KPL>(key, w, ss.bal, out, lst, kAmbCapWarp, n_in, n_amb, lane);
+  const int r = m - n_in;
+  bool complete = true;
+  if (n_amb == r || r == 0 || !w.refine) {
+    // every ambiguous candidate kept, none, or a tie at the cut without a usable bound
+    // (equal scores: the first r in index order)
+    emit_class(ss.bal, KPL, nullptr, true, true, 0, 0, m, 0, out, lane, r);
+    if (out_user != nullptr) emit_class(ss.bal, KPL, nullptr, true, true, 0, 0, m, 0, out_user, lane, r);
+  } else if (n_amb > kAmbCapWarp) {
+    // more ambiguous candidates than the list holds (clustered scores): the exact
+    // selection that re-reads the row instead of holding it
+    warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+    __syncwarp();
+    if (out_user != nullptr)
+      for (int i = lane; i <= m; i += 32) out_user[i] = out[i];
+  } else {
+    // the certain ones are in place: release them, the refine item does the rest
+    if (lane == 0) *meta = make_int2(n_in, n_amb);
+    __syncwarp();
+    if (lane == 0) st_release_gpu(ready, n_in + 1);
+    complete = false;
+  }
+  KIN_TOC(kTrCSelPass, t_p);
+  return complete;
 }
 
 // Selection of one row by all NW consumer warps: warp w holds candidates
@@ -651,10 +686,10 @@ __device__ void warp_select_bits(const float *srow, int n, int m, int nb, float 
 // kept list is written in index order: each warp offsets its own compaction by the counts
 // of the warps before it.
 template <int KPL, int NW, int D, typename Bar>
-__device__ void cta_select_row(const float *srow, int n, int m, int nb, float E,
+__device__ bool cta_select_row(const float *srow, int n, int m, int nb, float E,
                                const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
-                               const SelScratch &ss, int32_t *out) {
-  constexpr int kCap = kAmbCapCta;
+                               const SelScratch &ss, int32_t *out, int32_t *out_user,
+                               int32_t *ready, int2 *lst, int2 *meta) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int jbase = w * 32 * KPL;
   uint32_t key[KPL];
@@ -717,7 +752,7 @@ __device__ void cta_select_row(const float *srow, int n, int m, int nb, float E,
 #pragma unroll 1
     for (int b = top - 1; b >= 0 && cnt_t != m; --b) {
       const uint32_t cand = t | (1u << b);
-        int c0 = 0, c1 = 0;
+      int c0 = 0, c1 = 0;
 #pragma unroll
       for (int i = 0; i + 1 < KPL; i += 2) {
         c0 += key[i] >= cand ? 1 : 0;
@@ -734,49 +769,51 @@ __device__ void cta_select_row(const float *srow, int n, int m, int nb, float E,
     exact = cnt_t == m;
     return t;
   };
-  if (m > 0) {
-    bool exact;
-    const uint32_t t = threshold(exact);
-    const Window win = make_window(t, E);
-    uint32_t *bal = ss.bal + w * 2 * KPL;   // this warp's class ballots
-    int n_in_w, n_amb_w;
-    classify<KPL>(key, win, bal, n_in_w, n_amb_w, lane);
-    int in_before;
-    const int n_in = cta_sum(n_in_w, &in_before);
-    int amb_before;
-    const int n_amb = cta_sum(n_amb_w, &amb_before);
-    const int r = m - n_in;
-    if (n_amb == r) {
-      // every ambiguous candidate is kept: this warp's kept ones follow the earlier warps'
-      emit_kept(bal, KPL, nullptr, amb_before, in_before + amb_before, m, jbase, out, lane);
-    } else if (n_amb > kCap) {
-      // more ambiguous candidates than the list holds: warp 0 selects the row exactly,
-      // re-reading it from L2
-      if (w == 0) warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
-      return;
-    } else {
-      if (win.refine && w == 0) group_query<D>(qg, G, const_cast<float *>(rc.qs), lane);
-      list_amb(bal, KPL, amb_before, kCap, jbase, ss.lj, lane);
-      Bar::sync();   // the list and qs complete
-      if (win.refine) {
-        refine_listed<D, NW * 32>(rc, srow, ss.lj, ss.lr, n_amb, threadIdx.x, lane);
-      } else {
-        for (int e = threadIdx.x; e < n_amb; e += NW * 32) ss.lr[e] = 2u;
-      }
-      Bar::sync();
-      if (w == 0) {
-        if (n_amb <= 32 * 4)
-          choose_amb<4>(ss.lr, n_amb, r, ss.lf, lane);
-        else
-          choose_amb<kCap / 32>(ss.lr, n_amb, r, ss.lf, lane);
-      }
-      Bar::sync();
-      int kept_before;
-      cta_sum(kept_count(bal, KPL, ss.lf, amb_before, lane), &kept_before);
-      emit_kept(bal, KPL, ss.lf, amb_before, kept_before, m, jbase, out, lane);
-    }
+  if (threadIdx.x == 0) {
+    out[m] = nb - 1;
+    if (out_user != nullptr) out_user[m] = nb - 1;
   }
-  if (threadIdx.x == 0) out[m] = nb - 1;
+  if (m == 0) return true;
+  bool exact;
+  const uint32_t t = threshold(exact);
+  const Window win = make_window(t, E);
+  uint32_t *bal = ss.bal + w * 2 * KPL;   // this warp's class ballots
+  int n_in_w, n_amb_w;
+  classify<KPL>(key, win, bal, n_in_w, n_amb_w, lane);
+  int in_before;
+  const int n_in = cta_sum(n_in_w, &in_before);
+  int amb_before;
+  const int n_amb = cta_sum(n_amb_w, &amb_before);
+  const int r = m - n_in;
+  if (n_amb == r || r == 0 || !win.refine) {
+    // every ambiguous candidate kept, none, or a tie without a usable bound: the first r
+    // in index order; this warp's kept ones follow the earlier warps'
+    const int take_before = min(amb_before, r);
+    emit_class(bal, KPL, nullptr, true, true, amb_before, in_before + take_before, m, jbase, out,
+               lane, r);
+    if (out_user != nullptr)
+      emit_class(bal, KPL, nullptr, true, true, amb_before, in_before + take_before, m, jbase,
+                 out_user, lane, r);
+    return true;
+  }
+  if (n_amb > kAmbCapWarp) {
+    // more ambiguous candidates than the list holds: warp 0 selects the row exactly,
+    // re-reading it from L2
+    if (w == 0) {
+      warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+      __syncwarp();
+      if (out_user != nullptr)
+        for (int i = lane; i <= m; i += 32) out_user[i] = out[i];
+    }
+    return true;
+  }
+  // the certain ones in place, the ambiguous ones listed: release, the refine item does
+  // the rest
+  emit_in_and_list<KPL>(key, bal, in_before, amb_before, jbase, out, lst, kAmbCapWarp, lane);
+  if (threadIdx.x == 0) *meta = make_int2(n_in, n_amb);
+  Bar::sync();
+  if (threadIdx.x == 0) st_release_gpu(ready, n_in + 1);
+  return false;
 }
 
 // Kept blocks of one row by one warp for rows too long for the registers: radix select
@@ -902,12 +939,13 @@ __device__ __forceinline__ void fallback_kept(int m, int nb, int32_t *out, int t
 // ----------------------------------------------------------------------------------
 
 // Work queue order.  Round r (0 <= r < batch + lag_attn) holds, in this order, the score
-// items of sequence r, the select items of sequence r - lag_select and the attention items
-// of sequence r - lag_attn, each part only when that sequence exists.  Every item still
-// comes after everything it waits for (lag_attn >= lag_select >= 0), so a CTA that takes
-// items in queue order never waits on an item that no CTA has taken; the lags let the
-// score streaming of later sequences overlap the attention of earlier ones.
-enum : int { kItemScore = 0, kItemSelect = 1, kItemAttn = 2 };
+// items of sequence r, the select items of sequence r - lag_select, the refine items of
+// sequence r - lag_refine and the attention items of sequence r - lag_attn, each part only
+// when that sequence exists.  Every item still comes after everything it waits for
+// (lag_attn >= lag_refine >= lag_select >= 0), so a CTA that takes items in queue order
+// never waits on an item that no CTA has taken; the lags let the score streaming of later
+// sequences overlap the attention of earlier ones.
+enum : int { kItemScore = 0, kItemSelect = 1, kItemRefine = 2, kItemAttn = 3 };
 struct QueueItem {
   int kind;    // kItem*
   int local;   // index among the items of its kind, in sequence-major order
@@ -915,14 +953,16 @@ struct QueueItem {
 
 __device__ __forceinline__ int queue_before(const FusedParams &p, int r) {   // items in rounds < r
   const int B = p.batch;
-  const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B, a_per = p.n_attn_items / B;
+  const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B;
+  const int ref_per = p.n_refine_items / B, a_per = p.n_attn_items / B;
   return s_per * min(max(r, 0), B) + sel_per * min(max(r - p.lag_select, 0), B) +
-         a_per * min(max(r - p.lag_attn, 0), B);
+         ref_per * min(max(r - p.lag_refine, 0), B) + a_per * min(max(r - p.lag_attn, 0), B);
 }
 
 __device__ QueueItem queue_item(const FusedParams &p, int i) {
   const int B = p.batch;
-  const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B, a_per = p.n_attn_items / B;
+  const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B;
+  const int ref_per = p.n_refine_items / B, a_per = p.n_attn_items / B;
   int lo = 0, hi = B + p.lag_attn;   // the last round r in [lo, hi) with queue_before(r) <= i
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -937,6 +977,11 @@ __device__ QueueItem queue_item(const FusedParams &p, int i) {
   if (ss >= 0 && ss < B) {
     if (off < sel_per) return QueueItem{kItemSelect, ss * sel_per + off};
     off -= sel_per;
+  }
+  const int rs = lo - p.lag_refine;
+  if (rs >= 0 && rs < B) {
+    if (off < ref_per) return QueueItem{kItemRefine, rs * ref_per + off};
+    off -= ref_per;
   }
   return QueueItem{kItemAttn, (lo - p.lag_attn) * a_per + off};
 }
@@ -960,6 +1005,19 @@ __device__ bool make_desc(const FusedParams &p, QueueItem qi, Desc &d) {
     const int h0 = hr * HS, hs = min(HS, H - h0);
     const int pps = BfTile<D>::kStageBytes / (hs * D * 2);    // pages per stage
     d = Desc{kDescScore, 0, (npg + pps - 1) / pps, b, h0, j0, hs, L};
+    return true;
+  }
+  if (qi.kind == kItemRefine) {
+    // the ambiguous candidates left by the selections of (sequence, rows h0 .. h0 + hs)
+    const int per_seq = (H + kRefineRows - 1) / kRefineRows;
+    const int b = item / per_seq, r = item % per_seq;
+    const int L = __ldg(p.seq_lens + b);
+    if (L < 1 || L > kBlock * p.max_blocks) return false;
+    const int nb = (L + kBlock - 1) / kBlock;
+    if (nb <= p.top_k || p.top_k < 2) return false;             // no selection, or nothing to choose
+    const int h0 = r * kRefineRows;
+    const int hs = min(kRefineRows, H - h0);
+    d = Desc{kDescRefine, 0, 0, b, h0, nb - 1, hs, L};
     return true;
   }
   if (qi.kind == kItemSelect) {
@@ -1009,7 +1067,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
   const bool leader = q == 0;
   const uint64_t policy = l2_policy_evict_first();
   const int H = p.num_kv_heads;
-  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
+  const int total = p.n_score_items + p.n_select_items + p.n_refine_items + p.n_attn_items;
   uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
   uint32_t nd = 0;            // descriptors read (and, by the leader, pushed)
   uint32_t nq = 0;            // leader: score items whose q rows it staged
@@ -1145,6 +1203,109 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
                     policy);
         KIN_TOC(kTrPIssue, t_issue);
       }
+    } else if (d.kind == kDescRefine) {
+      // Rows h0 + hh, hh = q + kProducers k: once a row's selection has released its first
+      // phase, stage its listed ambiguous candidates, kRefinePerStage per ring stage: a
+      // header of (block, first-code score) entries written by the lanes, then the second
+      // centroid code of each candidate's page by a bulk copy.  Then an end marker to each
+      // consumer of this pipeline (the consumers cannot know the stage count).  The
+      // metadata and the first 64 entries of both rows are read at once, then all their
+      // pages, so that the item pays few memory latencies one after the other.
+      const int b = d.row, h0 = d.x0, hs = d.x2;
+      constexpr uint32_t kRowBytes = D * 2;
+      constexpr int kRows = kRefineRows / kProducers;
+      int v[kRows];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const int hh = q + kProducers * k;
+        v[k] = 0;
+        if (lane == 0 && hh < hs) v[k] = wait_flag_value(p.ready + b * H + h0 + hh, 1, sh, p.err);
+        v[k] = __shfl_sync(0xffffffffu, v[k], 0);
+      }
+      __syncwarp();   // the lanes read what the selections released after lane 0's acquire
+      int n_amb[kRows];
+      int2 ent[kRows][2];
+      int pgs[kRows][2];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const int row = b * H + h0 + q + kProducers * k;
+        const bool live = q + kProducers * k < hs && v[k] >= 1 && v[k] < kReadyAll;
+        const int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
+        n_amb[k] = live ? min(__ldcg(&p.amb_meta[row].y), kAmbCapWarp) : 0;
+        ent[k][0] = live ? __ldcg(lst + lane) : make_int2(-1, 0);
+        ent[k][1] = live ? __ldcg(lst + 32 + lane) : make_int2(-1, 0);
+      }
+      const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+      auto page_of = [&](int j) {
+        if (j < 0 || j >= p.max_blocks) return -1;
+        const int pp = __ldg(trow + j);
+        return pp >= 0 && pp < p.num_pages ? pp : -1;
+      };
+#pragma unroll
+      for (int k = 0; k < kRows; ++k)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) pgs[k][i] = 32 * i + lane < n_amb[k] ? page_of(ent[k][i].x) : -1;
+      int k_item = 0;
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        const int hh = q + kProducers * k;
+        const int row = b * H + h0 + hh;
+        const int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
+        for (int e0 = 0; e0 < n_amb[k]; e0 += kRefinePerStage) {
+          const int cnt = min(kRefinePerStage, n_amb[k] - e0);
+          const int e = e0 + lane;
+          // entry e: held by lane e % 32 in register e / 32 (first 64), else read now
+          const int src = e & 31;
+          const int2 e_lo = make_int2(__shfl_sync(0xffffffffu, ent[k][0].x, src),
+                                      __shfl_sync(0xffffffffu, ent[k][0].y, src));
+          const int2 e_hi = make_int2(__shfl_sync(0xffffffffu, ent[k][1].x, src),
+                                      __shfl_sync(0xffffffffu, ent[k][1].y, src));
+          const int p_lo = __shfl_sync(0xffffffffu, pgs[k][0], src);
+          const int p_hi = __shfl_sync(0xffffffffu, pgs[k][1], src);
+          int2 en = make_int2(-1, 0);
+          int pg = -1;
+          if (lane < cnt) {
+            if (e < 32) {
+              en = e_lo;
+              pg = p_lo;
+            } else if (e < 64) {
+              en = e_hi;
+              pg = p_hi;
+            } else {
+              en = __ldcg(lst + e);
+              pg = page_of(en.x);
+            }
+          }
+          const uint32_t vmask = __ballot_sync(0xffffffffu, pg >= 0);
+          const int cc = k_item % C::kPPC;
+          const uint32_t n = pos[cc];
+          const int s = R::slot(q + kProducers * cc, n);
+          if (lane == 0) wait_bar(&sh.empty[s], R::phase(n) ^ 1u, sh, p.err);
+          __syncwarp();
+          uint8_t *stage = ring + s * R::kStageBytes;
+          if (lane < cnt) reinterpret_cast<int2 *>(stage)[lane] = en;
+          fence_proxy_async_smem();   // later copies into this stage follow these writes
+          __syncwarp();
+          if (lane == 0) {
+            sh.meta[s] = make_int4(hh, e0, cnt, static_cast<int>(vmask));
+            if (vmask != 0)
+              mbar_arrive_expect_tx(&sh.full[s], __popc(vmask) * kRowBytes);
+            else
+              mbar_arrive(&sh.full[s]);
+          }
+          __syncwarp();
+          if (pg >= 0)
+            bulk_load(stage + 256 + lane * kRowBytes,
+                      p.cent_lo + (static_cast<int64_t>(pg) * H + h0 + hh) * D, kRowBytes,
+                      &sh.full[s], policy);
+          ++pos[cc];
+          ++k_item;
+        }
+      }
+      for (int cc = 0; cc < C::kPPC; ++cc) {
+        if (lane == 0) claim(cc, make_int4(-1, 0, 0, 0), 0u);
+        ++pos[cc];
+      }
     } else if (d.kind == kDescAttn) {
       // Pages i = q, q + kProducers, ... of the split: lane l reads page
       // i = base + l * kProducers, then the pages are staged in order.
@@ -1153,10 +1314,14 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       const int nb = (L + kBlock - 1) / kBlock;
       const bool every_block = (d.x2 & kAttnEveryBlock) != 0;
       const int i0 = d.x0 * p.items_per_split;
+      // entries [0, ready_v - 1) and the final block (entry top_k - 1) may be read once
+      // the row's ready word is ready_v; all of them at kReadyAll
+      int ready_v = kReadyAll;
       if (!every_block && q < cnt) {
         KIN_TIC(t0);
-        if (lane == 0) wait_flag(p.ready + row, 1, sh, p.err);
-        __syncwarp();
+        if (lane == 0) ready_v = wait_flag_value(p.ready + row, 1, sh, p.err);
+        ready_v = __shfl_sync(0xffffffffu, ready_v, 0);
+        __syncwarp();   // the lanes read the kept list after lane 0's acquire
         KIN_TOC(kTrPReady, t0);
 #ifdef KIN_TRACE_CYCLES
         if (lane == 0 && q == 0) KIN_ITEM_STAMP(d.item, 2, gtime());
@@ -1167,6 +1332,15 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
       const int32_t ybase = (row % H) * kBlock;
       for (int base = q; base < cnt; base += 32 * kProducers) {
         KIN_TIC(t_meta);
+        if (ready_v < kReadyAll) {
+          // this batch reads entries i0 + base .. i0 + base + 31 kProducers
+          const int e_lo = i0 + base, e_hi = i0 + min(cnt - 1, base + 31 * kProducers);
+          if (e_lo < p.top_k - 1 && e_hi >= ready_v - 1) {
+            if (lane == 0) ready_v = wait_flag_value(p.ready + row, kReadyAll, sh, p.err);
+            ready_v = __shfl_sync(0xffffffffu, ready_v, 0);
+            __syncwarp();
+          }
+        }
         const int i = base + lane * kProducers;
         int page = -1, ntok = 0;
         if (i < cnt) {
@@ -1600,31 +1774,27 @@ __device__ void consume_score(const FusedParams &p, const Desc &d, uint8_t *ring
 
 // Selection scratch: per selecting warp (one warp per row) kSelWarpBytes of the consumer
 // scratch; a cooperative selection uses the start of it for the whole CTA.
-constexpr int kSelWarpBytes = 4352;
+constexpr int kSelWarpBytes = 4096;
 static_assert(8 * kSelWarpBytes <= kScratchBytes, "per-warp selection scratch");
 static_assert(kSelWarpBytes % 16 == 0, "aligned per-warp regions");
 
 template <int D>
-__device__ __forceinline__ SelScratch sel_scratch(uint8_t *base, int cap, bool coop) {
+__device__ __forceinline__ SelScratch sel_scratch(uint8_t *base, bool coop) {
   SelScratch ss;
-  ss.xs = reinterpret_cast<int *>(base);                               // 128 ints
-  ss.qs = reinterpret_cast<float *>(base + 512);                       // D floats
-  ss.lj = reinterpret_cast<int *>(base + 512 + D * 4);                 // cap
-  ss.lr = reinterpret_cast<uint32_t *>(base + 512 + D * 4 + cap * 4);  // cap
-  ss.lf = base + 512 + D * 4 + cap * 8;                                // cap bytes
+  ss.xs = reinterpret_cast<int *>(base);                          // 128 ints
+  ss.qs = reinterpret_cast<float *>(base + 512);                  // D floats
+  ss.hist = reinterpret_cast<int *>(base + 512 + D * 4);          // 256 ints
   // class ballots: one warp: 2 x 64 slots in the xs area (a one-warp selection uses no
-  // cross-warp sums); cooperative: 8 warps x 2 x 16 slots after the lists
-  ss.bal = coop ? reinterpret_cast<uint32_t *>(base + 512 + D * 4 + cap * 9)
+  // cross-warp sums); cooperative: 8 warps x 2 x 16 slots after the histogram
+  ss.bal = coop ? reinterpret_cast<uint32_t *>(base + 512 + D * 4 + 1024)
                 : reinterpret_cast<uint32_t *>(base);
-  ss.hist = ss.lj;   // 256 ints: the long-row selection does not use the list
   return ss;
 }
-static_assert(512 + 128 * 4 + kAmbCapWarp * 9 <= kSelWarpBytes, "per-warp selection scratch");
+static_assert(512 + 128 * 4 + 1024 <= kSelWarpBytes, "per-warp selection scratch");
 static_assert(2 * 64 * 4 <= 512, "per-warp class ballots in the xs area");
-static_assert(512 + 128 * 4 + kAmbCapCta * 9 + 8 * 2 * 16 * 4 <= kScratchBytes,
-              "cooperative selection scratch");
-static_assert((kAmbCapCta * 9) % 4 == 0, "aligned cooperative ballots");
-static_assert(kAmbCapWarp >= 256, "the radix histogram shares the list");
+static_assert(512 + 128 * 4 + 1024 + 8 * 2 * 16 * 4 <= kScratchBytes, "cooperative selection scratch");
+static_assert(kRefineRows * kAmbCapWarp * 9 + 8 * (kRefineRows / kProducers) * 128 * 4 <= kScratchBytes,
+              "refine item scratch");
 
 template <int D, int NT>
 __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scratch,
@@ -1652,57 +1822,227 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
     const int row = b * H + h0;
     const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
     int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
-    const SelScratch ss = sel_scratch<D>(scratch, kAmbCapCta, true);
+    int32_t *out_user = p.sel_out == nullptr ? nullptr : p.sel_out + static_cast<int64_t>(row) * p.top_k;
+    const SelScratch ss = sel_scratch<D>(scratch, true);
     const float E = __uint_as_float(__ldcg(p.bound + row));
     const RefineCtx rc{p.cent_lo + h0 * D, trow, static_cast<int64_t>(H) * D, p.num_pages, ss.qs};
     const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h0 * G) * D;
     using Bar = typename C::Bar;
-    if (!ok)
+    int32_t *ready = p.ready + row;
+    int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
+    int2 *meta = p.amb_meta + row;
+    bool complete = true;
+    if (!ok) {
       fallback_kept(m, nb, out, tid, C::kCThreads);
-    else if (n <= NW * 32 * 2)
-      cta_select_row<2, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
-    else if (n <= NW * 32 * 4)
-      cta_select_row<4, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
-    else if (n <= NW * 32 * 8)
-      cta_select_row<8, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
-    else if (n <= NW * 32 * 16)
-      cta_select_row<16, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out);
-    else if (warp == 0)   // longer rows: one warp, radix select over L2
+      if (out_user != nullptr) fallback_kept(m, nb, out_user, tid, C::kCThreads);
+    } else if (n <= NW * 32 * 2) {
+      complete = cta_select_row<2, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+    } else if (n <= NW * 32 * 4) {
+      complete = cta_select_row<4, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+    } else if (n <= NW * 32 * 8) {
+      complete = cta_select_row<8, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+    } else if (n <= NW * 32 * 16) {
+      complete = cta_select_row<16, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+    } else if (warp == 0) {   // longer rows: one warp, radix select over L2
       warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+      __syncwarp();
+      if (out_user != nullptr)
+        for (int i = lane; i <= m; i += 32) out_user[i] = out[i];
+    }
     C::Bar::sync();
-    if (tid == 0) st_release_gpu(p.ready + row, 1);
+    if (tid == 0 && complete) st_release_gpu(ready, kReadyAll);
     KIN_TOC(kTrCSelComp, t_sel);
     C::Bar::sync();   // the scratch is reused by the next item
     if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
     return;
   }
-  const SelScratch ss = sel_scratch<D>(scratch + warp * kSelWarpBytes, kAmbCapWarp, false);
+  const SelScratch ss = sel_scratch<D>(scratch + warp * kSelWarpBytes, false);
   KIN_TIC(t_sel);
   for (int hh = warp; hh < hs; hh += C::kCW) {
     const int h = h0 + hh;
     const int row = b * H + h;
     const float *srow = p.scores + static_cast<int64_t>(row) * p.max_blocks;
     int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
+    int32_t *out_user = p.sel_out == nullptr ? nullptr : p.sel_out + static_cast<int64_t>(row) * p.top_k;
+    int32_t *ready = p.ready + row;
     const float E = __uint_as_float(__ldcg(p.bound + row));
     const RefineCtx rc{p.cent_lo + h * D, trow, static_cast<int64_t>(H) * D, p.num_pages, ss.qs};
     const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h * G) * D;
-    if (!ok)
+    int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
+    int2 *meta = p.amb_meta + row;
+    bool complete = true;
+    if (!ok) {
       fallback_kept(m, nb, out, lane, 32);
-    else if (n <= 32 * 16)
-      warp_select_bits<16, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
-    else if (n <= 32 * 32)
-      warp_select_bits<32, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
-    else if (n <= 32 * 64)
-      warp_select_bits<64, D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane KIN_TRACE_ARG);
-    else
+      if (out_user != nullptr) fallback_kept(m, nb, out_user, lane, 32);
+    } else if (n <= 32 * 16) {
+      complete = warp_select_bits<16, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+    } else if (n <= 32 * 32) {
+      complete = warp_select_bits<32, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+    } else if (n <= 32 * 64) {
+      complete = warp_select_bits<64, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+    } else {
       warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
+      __syncwarp();
+      if (out_user != nullptr)
+        for (int i = lane; i <= m; i += 32) out_user[i] = out[i];
+    }
     __syncwarp();
-    if (lane == 0) st_release_gpu(p.ready + row, 1);
+    if (lane == 0 && complete) st_release_gpu(ready, kReadyAll);
     __syncwarp();
   }
   KIN_TOC(kTrCSelComp, t_sel);
   C::Bar::sync();   // the scratch is reused by the next item
   if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
+}
+
+// The row's kept list in ascending order into dst[0 .. m): the certain candidates
+// in_list[0 .. n_in) (ascending, global memory) merged with the chosen ambiguous ones
+// ch[0 .. r) (ascending, shared memory); lane l merges the block indices in
+// [l span, (l + 1) span).  Only for the caller's copy of the kept lists.
+__device__ void merge_kept(const int32_t *in_list, int n_in, const int *ch, int r, int nmax,
+                           int32_t *dst, int lane) {
+  const int span = (nmax + 31) / 32;
+  const int v0 = min(nmax, lane * span), v1 = min(nmax, v0 + span);
+  auto lb_in = [&](int v) {
+    int lo = 0, hi = n_in;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldcg(in_list + mid) < v) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  };
+  auto lb_ch = [&](int v) {
+    int lo = 0, hi = r;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (ch[mid] < v) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  };
+  int i = lb_in(v0), k = lb_ch(v0);
+  const int i1 = lb_in(v1), k1 = lb_ch(v1);
+  int pos = i + k;
+  while (i < i1 || k < k1) {
+    const int a = i < i1 ? __ldcg(in_list + i) : 0x7fffffff;
+    const int c = k < k1 ? ch[k] : 0x7fffffff;
+    if (a < c) {
+      dst[pos++] = a;
+      ++i;
+    } else {
+      dst[pos++] = c;
+      ++k;
+    }
+  }
+}
+
+// A refine item: the ambiguous candidates that the selections of rows h0 .. h0 + hs - 1
+// left, re-scored with both centroid codes (s + qs . c2), the best m - n_in of them chosen
+// (equal keys to the lower block index) and appended to each row's kept list, which is
+// then released whole.  Consumer warp w takes the stages of its pipeline (rows
+// hh = q, q + kProducers, ...) until its end marker; one warp per row then chooses.
+template <int D, int NT>
+__device__ void consume_refine(const FusedParams &p, const Desc &d, uint8_t *ring, uint8_t *scratch,
+                               FusedShared &sh, uint32_t &n) {
+  using R = Ring<D, NT>;
+  using C = Cfg<D, NT>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = warp % kProducers;
+  const int H = p.num_kv_heads, G = p.group;
+  const int b = d.row, h0 = d.x0, hs = d.x2, nb = d.x1 + 1, m = p.top_k - 1;
+  constexpr int kCap = kAmbCapWarp;
+  uint32_t *lr = reinterpret_cast<uint32_t *>(scratch);                   // [kRefineRows][kCap]
+  int *lj = reinterpret_cast<int *>(scratch + kRefineRows * kCap * 4);     // [kRefineRows][kCap]
+  uint8_t *lf = scratch + kRefineRows * kCap * 8;                          // [kRefineRows][kCap]
+  float *qsw = reinterpret_cast<float *>(scratch + kRefineRows * kCap * 9) +
+               warp * (kRefineRows / kProducers) * D;
+  // the group-summed queries of this warp's rows
+  for (int k = 0, hh = q; hh < hs; ++k, hh += kProducers)
+    group_query<D>(p.q + (static_cast<int64_t>(b) * H * G + (h0 + hh) * G) * D, G, qsw + k * D, lane);
+  __syncwarp();
+  while (true) {
+    const int s = R::slot(warp, n);
+    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
+    ++n;
+    const int4 meta = sh.meta[s];
+    if (!ok || meta.x < 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[s]);
+      break;
+    }
+    const int hh = meta.x, e0 = meta.y, cnt = meta.z;
+    const uint32_t vmask = static_cast<uint32_t>(meta.w);
+    const uint8_t *stage = ring + s * R::kStageBytes;
+    if (lane < cnt) {
+      const int2 ent = reinterpret_cast<const int2 *>(stage)[lane];
+      float corr = 0.f;
+      if ((vmask >> lane) & 1u) {
+        // the lane's row is 2 D bytes from its neighbour's: read its 16-byte chunks in an
+        // order rotated by the lane, so that the lanes of a read hit distinct bank groups
+        const float *qs = qsw + (hh / kProducers) * D;
+        const uint4 *c2 = reinterpret_cast<const uint4 *>(stage + 256 + lane * D * 2);
+        constexpr int kCh = D / 8;
+#pragma unroll
+        for (int c = 0; c < kCh; ++c) {
+          const int cr = (c + lane) & (kCh - 1);
+          float f[8];
+          Elem<__nv_bfloat16>::unpack(c2[cr], f);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) corr = fmaf(qs[8 * cr + k], f[k], corr);
+        }
+      }
+      lr[hh * kCap + e0 + lane] = max(score_key(__int_as_float(ent.y) + corr), 2u);
+      lj[hh * kCap + e0 + lane] = ent.x;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.empty[s]);
+  }
+  C::Bar::sync();   // every listed candidate re-scored
+  const unsigned lt = (1u << lane) - 1u;
+  for (int hh = warp; hh < hs; hh += C::kCW) {
+    const int row = b * H + h0 + hh;
+    int v = 0;
+    if (lane == 0) v = ld_acquire_gpu(p.ready + row);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    __syncwarp();
+    if (v < 1 || v >= kReadyAll) continue;
+    const int2 mt = __ldcg(p.amb_meta + row);
+    const int n_in = mt.x, n_amb = min(mt.y, kCap), r = m - n_in;
+    if (n_amb <= r || r <= 0) {   // nothing to choose (not left by a selection): release
+      if (lane == 0) st_release_gpu(p.ready + row, kReadyAll);
+      continue;
+    }
+    if (n_amb <= 64)
+      choose_amb<2>(lr + hh * kCap, n_amb, r, lf + hh * kCap, lane);
+    else
+      choose_amb<kCap / 32>(lr + hh * kCap, n_amb, r, lf + hh * kCap, lane);
+    __syncwarp();
+    // the chosen ones in index order: after the certain ones in the kept list, and
+    // compacted into lr (no longer needed) for the caller's ascending copy
+    int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
+    int *ch = reinterpret_cast<int *>(lr + hh * kCap);
+    int written = 0;
+    for (int e0 = 0; e0 < n_amb; e0 += 32) {
+      const int e = e0 + lane;
+      const bool pick = e < n_amb && lf[hh * kCap + e] != 0;
+      const int j = pick ? lj[hh * kCap + e] : 0;
+      const unsigned km = __ballot_sync(0xffffffffu, pick);
+      const int at = written + __popc(km & lt);
+      __syncwarp();
+      if (pick && at < r) {
+        out[n_in + at] = j;
+        ch[at] = j;
+      }
+      written += __popc(km);
+    }
+    __syncwarp();
+    if (p.sel_out != nullptr) {
+      merge_kept(out, n_in, ch, min(written, r), nb - 1,
+                 p.sel_out + static_cast<int64_t>(row) * p.top_k, lane);
+    }
+    __syncwarp();
+    if (lane == 0) st_release_gpu(p.ready + row, kReadyAll);
+  }
+  C::Bar::sync();   // the scratch is reused by the next item
 }
 
 template <int D, int NT>
@@ -1718,10 +2058,10 @@ __device__ void consume_attention(const FusedParams &p, const Desc &d, uint8_t *
   const int row = d.row, split = d.x0, splits = d.x1, flags = d.x2, L = d.x3, cnt = d.count;
   const int b = row / H, h = row % H;
   const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, G, H};
-  if (p.top_k > 0 && (flags & kAttnEveryBlock) && split == 0) {
+  if (p.top_k > 0 && p.sel_out != nullptr && (flags & kAttnEveryBlock) && split == 0) {
     // no selection ran for this row: its kept list is every block, -1 padded
     const int nb = (L + kBlock - 1) / kBlock;
-    int32_t *srow = p.sel + static_cast<int64_t>(row) * p.top_k;
+    int32_t *srow = p.sel_out + static_cast<int64_t>(row) * p.top_k;
     for (int i = tid; i < p.top_k; i += C::kCThreads) srow[i] = i < nb ? i : -1;
   }
   KIN_TIC(t_q);
@@ -1844,6 +2184,8 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
       KIN_TIC(t0);
       consume_select<D, NT>(p, d, scratch, sh KIN_TRACE_ARG);
       KIN_TOC(kTrCSelect, t0);
+    } else if (d.kind == kDescRefine) {
+      consume_refine<D, NT>(p, d, ring, scratch, sh, n);
     } else if (d.kind == kDescAttn) {
       consume_attention<D, NT>(p, d, ring, scratch, sh, n KIN_TRACE_ARG);
     } else {   // kDescEmptyRow: a sequence whose length is out of range
@@ -1852,8 +2194,8 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
       const EmitCtx ec{p.out, p.lse, p.part_o, p.part_ml, p.attn_cnt, p.splits_per_row, p.group, H};
       write_empty_row<__nv_bfloat16, D, C::kCThreads>(ec, b, h);
       if (tid == 0 && h == 0) flag_error(p.err, KIN_DEVERR_SEQ_LEN);
-      if (p.top_k > 0) {
-        int32_t *srow = p.sel + static_cast<int64_t>(d.row) * p.top_k;
+      if (p.top_k > 0 && p.sel_out != nullptr) {
+        int32_t *srow = p.sel_out + static_cast<int64_t>(d.row) * p.top_k;
         for (int i = tid; i < p.top_k; i += C::kCThreads) srow[i] = -1;
       }
     }
@@ -1942,7 +2284,7 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
     ctas = sms * (occupancy < 1 ? 1 : occupancy);
     if (dev >= 0 && dev < kMaxDevices) resident[dev].store(ctas, std::memory_order_release);
   }
-  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
+  const int total = p.n_score_items + p.n_select_items + p.n_refine_items + p.n_attn_items;
   const int grid = min(total, ctas);
   if (grid <= 0) return cudaSuccess;
   fused_decode_kernel<D, NT><<<grid, C::kAllThreads, smem, stream>>>(*kmap, *vmap, p);
@@ -1952,6 +2294,8 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
 }  // namespace
 
 int fused_max_score_chunk() { return kMaxScoreChunk; }
+int fused_amb_cap() { return kAmbCapWarp; }
+int fused_refine_rows() { return kRefineRows; }
 
 #ifdef KIN_TRACE_CYCLES
 // Copy out (and clear) the cycle counters: [CTA][warp][slot], 160 x 12 x 20 words.

@@ -14,7 +14,7 @@
 
 namespace {
 
-constexpr size_t kStaticScratchBytes = 16u << 20;   // 16 MiB per GPU
+constexpr size_t kStaticScratchBytes = 32u << 20;   // 32 MiB per GPU
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];

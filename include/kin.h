@@ -194,8 +194,8 @@ KIN_API kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_
  * afterwards, or a loop that must not let cudaMalloc/cudaFree synchronise the device.
  * The paper has no counterpart: this is a property of the library, not of the method.
  * Identical work and results; args->workspace / workspace_bytes are ignored and the
- * scratch is instead a 16 MiB array inside the library, which every GPU that loads the
- * library keeps until the process exits.  Shapes whose kin_workspace_size exceeds 16 MiB
+ * scratch is instead a 32 MiB array inside the library, which every GPU that loads the
+ * library keeps until the process exits.  Shapes whose kin_workspace_size exceeds 32 MiB
  * return KIN_ERR_WORKSPACE.  The first call on a device looks up the array's device
  * address (with that device current); make that first call before any stream capture.
  * All calls share the one array, which starts zero-filled and keeps the previous call's
