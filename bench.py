@@ -736,19 +736,19 @@ def main() -> int:
     W, cfg = workload(args)
     cfg = replica_config(cfg, int(os.environ.get("RANK", "0")))
     inp = W.generate(cfg)
-    pool = None
-    if int(os.environ.get("RANK", "0")) == 0 and not args.no_cpu_baseline:
-        pool = OraclePool(inp, host_cores())      # forked before the first CUDA call
-    cx = Ctx()
-    loop = cfg.ctx_kind == "best_of_n" and cfg.steps > 1
-    runner = run_loop if loop else run_single
-    r, dw = runner(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e, inp)
     cpu = None
-    if pool is not None:
+    if int(os.environ.get("RANK", "0")) == 0 and not args.no_cpu_baseline:
+        # The oracle on the host cores, before this process touches the GPU: its workers
+        # are forked before the first CUDA call and run while nothing else does.
+        pool = OraclePool(inp, host_cores())
         try:
             cpu = cpu_baseline(pool, inp, args.cpu_seconds)
         finally:
             pool.close()
+    cx = Ctx()
+    loop = cfg.ctx_kind == "best_of_n" and cfg.steps > 1
+    runner = run_loop if loop else run_single
+    r, dw = runner(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e, inp)
     trec = traffic_record(describe(cfg))
     del dw
     torch.cuda.empty_cache()

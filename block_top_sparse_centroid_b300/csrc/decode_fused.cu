@@ -65,8 +65,6 @@ constexpr int kDescs = 8;                           // descriptor slots producer
 constexpr int kMaxScoreChunk = 256;                 // candidate blocks per score item
 constexpr int kHeadsPerRange = 32;                  // KV heads per score / select item
 constexpr int kScoreSlots = 16;                     // score-item arrival counters (> kDescs)
-constexpr int kRefineRows = 8;                      // rows per refine item (one warp each)
-constexpr int kRefinePerStage = 28;                 // ambiguous candidates per refine ring stage
 // Consumer scratch: the combine buffers of an attention item, the group-summed queries
 // of a score item, or the histograms of the selections (never at once).
 constexpr int kScratchBytes = 34 * 1024;
@@ -109,9 +107,6 @@ struct Ring {
   __device__ static __forceinline__ uint32_t phase(uint32_t n) { return (n / kPer) & 1u; }
 };
 
-static_assert(256 + kRefinePerStage * 128 * 2 <= BfTile<128>::kStageBytes, "refine stage, d = 128");
-static_assert(256 + kRefinePerStage * 64 * 2 <= BfTile<64>::kStageBytes, "refine stage, d = 64");
-static_assert(kRefinePerStage * 8 <= 256, "refine stage header");
 
 // Score items of up to 8 heads and groups of up to 8 query heads (NT = 1) get their raw q
 // rows staged by a bulk copy into one of two slots, so that no consumer waits on a global
@@ -126,8 +121,7 @@ constexpr size_t fused_smem_bytes() {
   return 1024 + Ring<D, NT>::kBytes + kScratchBytes + q_stage_bytes<NT>();
 }
 
-enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4,
-             kDescRefine = 5 };
+enum : int { kDescEnd = 0, kDescScore = 1, kDescSelect = 2, kDescAttn = 3, kDescEmptyRow = 4 };
 enum : int { kAttnEveryBlock = 1, kAttnAppendLast = 2 };
 
 // A work item as the producer hands it to the consumers.
@@ -313,7 +307,7 @@ __device__ __forceinline__ float key_score(uint32_t k) {
 // the kept list.  Keys of real scores are >= 2, padding slots 0.
 // ----------------------------------------------------------------------------------
 constexpr uint32_t kKeyIn = 0xffffffffu;   // above the key of every number (+inf: 0xff800000)
-// Ambiguous candidates a row's selection can list for its refine item.
+// Ambiguous candidates a row's selection re-scores in shared memory (more: the long-row path).
 constexpr int kAmbCapWarp = 256;
 
 struct Window {
@@ -547,14 +541,14 @@ __device__ __forceinline__ void emit_in_and_list(const uint32_t (&key)[KPL], con
 }
 
 // Choose r of the na listed ambiguous candidates (ranks 0 .. na - 1, in index order) by
-// one warp: the r largest re-scored keys lr[], equal keys to the lower rank.  Sets lf[rank]
-// (1 = kept) for every rank.  KA keys per lane: na <= 32 KA.
-template <int KA>
+// one warp: the r largest re-scored keys lr[rank * KS], equal keys to the lower rank.  Sets
+// lf[rank] (1 = kept) for every rank.  KA keys per lane: na <= 32 KA.
+template <int KA, int KS = 1>
 __device__ __forceinline__ void choose_amb(const uint32_t *lr, int na, int r, uint8_t *lf,
                                            int lane) {
   uint32_t key[KA];
 #pragma unroll
-  for (int i = 0; i < KA; ++i) key[i] = lane + 32 * i < na ? lr[lane + 32 * i] : 0u;
+  for (int i = 0; i < KA; ++i) key[i] = lane + 32 * i < na ? lr[(lane + 32 * i) * KS] : 0u;
   bool exact;
   const uint32_t t = bits_threshold<KA>(key, r, exact);
   int take_eq = 0;
@@ -600,21 +594,102 @@ __device__ __forceinline__ void emit_class(const uint32_t *bal, int nslots, cons
   }
 }
 
+#ifndef KIN_RK_ROWS
+#define KIN_RK_ROWS 16   // candidate rows per re-scoring batch of one warp (no spill at d = 128)
+#endif
+// Pages of the listed ambiguous candidates lst[e].x into pg[e] (-1: outside the table or
+// an invalid page id), e = ti, ti + nthr, ...; several loads in flight per thread.
+__device__ __forceinline__ void list_pages(const int2 *lst, int n, const int32_t *trow,
+                                           int max_blocks, int64_t num_pages, int *pg, int ti,
+                                           int nthr) {
+#pragma unroll 4
+  for (int e = ti; e < n; e += nthr) {
+    const int j = lst[e].x;
+    const int pp = j >= 0 && j < max_blocks ? __ldg(trow + j) : -1;
+    pg[e] = pp >= 0 && pp < num_pages ? pp : -1;
+  }
+}
+
+// Re-scored keys of the listed ambiguous candidates lst[e] = (j, first-code score bits),
+// e in batches of KIN_RK_ROWS starting at e_begin, e_step apart (one warp): lst[e].y becomes the
+// key of s + qs . c2_j.  Each candidate row is read by D / 8 lanes, one 16-byte chunk each
+// (lane chunk c: dimensions 8c .. 8c + 7, whose qs values the lane keeps in registers),
+// and all loads of a batch are issued before any is used, so a batch costs one memory
+// latency.
+template <int D>
+__device__ __forceinline__ void refine_keys(int2 *lst, const int *pg, int n, int e_begin,
+                                            int e_step, const __nv_bfloat16 *c2, int64_t stride,
+                                            const float *qs, int lane) {
+  constexpr int kLpr = D / 8;        // lanes per candidate row
+  constexpr int kRpi = 32 / kLpr;    // rows per warp-wide load
+  constexpr int kNld = KIN_RK_ROWS / kRpi;    // loads per lane per batch
+  const int c = lane % kLpr, sub = lane / kLpr;
+  float qv[8];
+  {
+    const float4 a = *reinterpret_cast<const float4 *>(qs + 8 * c);
+    const float4 b = *reinterpret_cast<const float4 *>(qs + 8 * c + 4);
+    qv[0] = a.x; qv[1] = a.y; qv[2] = a.z; qv[3] = a.w;
+    qv[4] = b.x; qv[5] = b.y; qv[6] = b.z; qv[7] = b.w;
+  }
+#pragma unroll 1
+  for (int e0 = e_begin; e0 < n; e0 += e_step) {
+    uint4 raw[kNld];
+#pragma unroll
+    for (int k = 0; k < kNld; ++k) {
+      const int e = e0 + k * kRpi + sub;
+      const int pgv = e < n ? pg[e] : -1;
+      raw[k] = pgv >= 0 ? __ldcg(reinterpret_cast<const uint4 *>(c2 + pgv * stride) + c)
+                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int k = 0; k < kNld; ++k) {
+      float f[8];
+      Elem<__nv_bfloat16>::unpack(raw[k], f);
+      float part = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) part = fmaf(qv[i], f[i], part);
+#pragma unroll
+      for (int o = 1; o < kLpr; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      const int e = e0 + k * kRpi + sub;
+      if (c == 0 && e < n)
+        lst[e].y = static_cast<int>(max(score_key(__int_as_float(lst[e].y) + part), 2u));
+    }
+  }
+}
+
+// The chosen ambiguous candidates (lf[e] != 0) in index order into dst[0 .. r), one warp.
+__device__ __forceinline__ void append_chosen(const int2 *lst, const uint8_t *lf, int n, int r,
+                                              int32_t *dst, int lane) {
+  const unsigned lt = (1u << lane) - 1u;
+  int written = 0;
+  for (int e0 = 0; e0 < n; e0 += 32) {
+    const int e = e0 + lane;
+    const bool pick = e < n && lf[e] != 0;
+    const unsigned km = __ballot_sync(0xffffffffu, pick);
+    const int at = written + __popc(km & lt);
+    if (pick && at < r) dst[at] = lst[e].x;
+    written += __popc(km);
+  }
+}
+
 // Kept lists are released in two phases (the row's ready word): first the candidates that
 // are in for certain (positions 0 .. n_in - 1, ascending) and the final block (position m),
-// ready word n_in + 1, by the selection; then the chosen ambiguous ones (positions
-// n_in .. m - 1, ascending), ready word kReadyAll, by the row's refine item.  The attention
-// streams the first part meanwhile.  A selection that settles its row itself (no
-// ambiguous candidate to re-score) releases kReadyAll at once.  The caller's copy
-// (sel_out) is ascending.
+// ready word n_in + 1, as soon as they are classified; then, once the ambiguous ones are
+// re-scored, the chosen ones (positions n_in .. m - 1, ascending), ready word kReadyAll.
+// The attention streams the first part meanwhile.  A selection with no ambiguous
+// candidate to re-score releases kReadyAll at once.  The caller's copy (sel_out) is
+// ascending.
 constexpr int kReadyAll = 1 << 30;
 
 // Scratch of one selecting warp (or of the CTA in a cooperative selection).
 struct SelScratch {
-  float *qs;      // [D] group-summed query (rows too long for the registers)
+  float *qs;      // [D] group-summed query of the row
   uint32_t *bal;  // [2 * slots] class ballots of the warp (cooperative: per warp)
   int *hist;      // [256] radix histograms (rows too long for the registers)
   int *xs;        // [128] cross-warp partial sums (cooperative selection)
+  int2 *lst;      // [kAmbCapWarp] listed ambiguous candidates (block, score bits / key)
+  int *pg;        // [kAmbCapWarp] their pages
+  uint8_t *lf;    // [kAmbCapWarp] chosen flags
 };
 
 template <int D>
@@ -624,14 +699,13 @@ __device__ void warp_select_long(const float *srow, int n, int m, int nb, float 
 
 // Kept blocks of one row by one warp, keys in registers: lane l holds candidates
 // j = l + 32 i, i < KPL (n <= 32 KPL).  Writes the kept list out[0 .. m] (the final block
-// nb - 1 at out[m]) and returns true when the row is settled; returns false after the
-// first release phase, leaving the ambiguous candidates (lst, meta) to the row's refine
-// item.
+// nb - 1 at out[m]), releasing the certain candidates before it re-scores the ambiguous
+// ones (lst, this warp's shared memory); returns true (the row is settled).
 template <int KPL, int D>
 __device__ bool warp_select_bits(const float *srow, int n, int m, int nb, float E,
                                  const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
                                  const SelScratch &ss, int32_t *out, int32_t *out_user,
-                                 int32_t *ready, int2 *lst, int2 *meta, int lane KIN_TRACE_PARAM) {
+                                 int32_t *ready, int2 *lst, int lane KIN_TRACE_PARAM) {
   KIN_TIC(t_k);
   uint32_t key[KPL];
   const int nv = n > lane ? (n - lane + 31) / 32 : 0;   // this lane's candidates
@@ -639,6 +713,7 @@ __device__ bool warp_select_bits(const float *srow, int n, int m, int nb, float 
     float sv[KPL];   // every load issued before any is used
 #pragma unroll
     for (int i = 0; i < KPL; ++i) sv[i] = i < nv ? __ldcg(srow + lane + 32 * i) : 0.f;
+    group_query<D>(qg, G, ss.qs, lane);   // for the re-scoring; its loads overlap these
 #pragma unroll
     for (int i = 0; i < KPL; ++i) key[i] = i < nv ? max(score_key(sv[i]), 2u) : 0u;
   }
@@ -669,11 +744,23 @@ __device__ bool warp_select_bits(const float *srow, int n, int m, int nb, float 
     if (out_user != nullptr)
       for (int i = lane; i <= m; i += 32) out_user[i] = out[i];
   } else {
-    // the certain ones are in place: release them, the refine item does the rest
-    if (lane == 0) *meta = make_int2(n_in, n_amb);
+    // the certain ones are in place: release them, then re-score the listed ambiguous
+    // candidates (their pages from the block table, then their second codes: two memory
+    // latencies per 32 of them), choose r and append them
     __syncwarp();
     if (lane == 0) st_release_gpu(ready, n_in + 1);
-    complete = false;
+    list_pages(lst, n_amb, rc.trow, n, rc.num_pages, ss.pg, lane, 32);
+    __syncwarp();
+    refine_keys<D>(lst, ss.pg, n_amb, 0, KIN_RK_ROWS, rc.c2, rc.stride, ss.qs, lane);
+    __syncwarp();
+    const uint32_t *lr = reinterpret_cast<const uint32_t *>(lst) + 1;
+    if (n_amb <= 64)
+      choose_amb<2, 2>(lr, n_amb, r, ss.lf, lane);
+    else
+      choose_amb<kAmbCapWarp / 32, 2>(lr, n_amb, r, ss.lf, lane);
+    __syncwarp();
+    append_chosen(lst, ss.lf, n_amb, r, out + n_in, lane);
+    if (out_user != nullptr) emit_class(ss.bal, KPL, ss.lf, true, true, 0, 0, m, 0, out_user, lane);
   }
   KIN_TOC(kTrCSelPass, t_p);
   return complete;
@@ -689,7 +776,7 @@ template <int KPL, int NW, int D, typename Bar>
 __device__ bool cta_select_row(const float *srow, int n, int m, int nb, float E,
                                const RefineCtx &rc, const __nv_bfloat16 *qg, int G,
                                const SelScratch &ss, int32_t *out, int32_t *out_user,
-                               int32_t *ready, int2 *lst, int2 *meta) {
+                               int32_t *ready, int2 *lst) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int jbase = w * 32 * KPL;
   uint32_t key[KPL];
@@ -703,6 +790,7 @@ __device__ bool cta_select_row(const float *srow, int n, int m, int nb, float E,
 #pragma unroll
     for (int i = 0; i < KPL; ++i) key[i] = jbase + lane + 32 * i < n ? max(score_key(sv[i]), 2u) : 0u;
   }
+  if (w == 0) group_query<D>(qg, G, ss.qs, lane);   // published by the first CTA sum's barrier
   int *xs = ss.xs;
   int par = 0;
   // sum of v over the consumer warps (v must be warp-uniform); *before = the sum over the
@@ -807,13 +895,34 @@ __device__ bool cta_select_row(const float *srow, int n, int m, int nb, float E,
     }
     return true;
   }
-  // the certain ones in place, the ambiguous ones listed: release, the refine item does
-  // the rest
   emit_in_and_list<KPL>(key, bal, in_before, amb_before, jbase, out, lst, kAmbCapWarp, lane);
-  if (threadIdx.x == 0) *meta = make_int2(n_in, n_amb);
+  // the certain ones in place: release them; the ambiguous ones listed: every warp
+  // re-scores KIN_RK_ROWS of them at a time (one memory latency after the page lookup),
+  // warp 0 chooses r and appends them, every warp merges its part of the caller's
+  // ascending copy
   Bar::sync();
   if (threadIdx.x == 0) st_release_gpu(ready, n_in + 1);
-  return false;
+  list_pages(lst, n_amb, rc.trow, n, rc.num_pages, ss.pg, threadIdx.x, NW * 32);
+  Bar::sync();
+  refine_keys<D>(lst, ss.pg, n_amb, KIN_RK_ROWS * w, KIN_RK_ROWS * NW, rc.c2, rc.stride, ss.qs, lane);
+  Bar::sync();
+  if (w == 0) {
+    const uint32_t *lr = reinterpret_cast<const uint32_t *>(lst) + 1;
+    if (n_amb <= 64)
+      choose_amb<2, 2>(lr, n_amb, r, ss.lf, lane);
+    else
+      choose_amb<kAmbCapWarp / 32, 2>(lr, n_amb, r, ss.lf, lane);
+    __syncwarp();
+    append_chosen(lst, ss.lf, n_amb, r, out + n_in, lane);
+  }
+  Bar::sync();
+  if (out_user != nullptr) {
+    int cb = 0;   // chosen among the ambiguous candidates of the warps before this one
+    for (int e = lane; e < amb_before; e += 32) cb += ss.lf[e] != 0 ? 1 : 0;
+    cb = static_cast<int>(__reduce_add_sync(0xffffffffu, static_cast<unsigned>(cb)));
+    emit_class(bal, KPL, ss.lf, true, true, amb_before, in_before + cb, m, jbase, out_user, lane);
+  }
+  return true;
 }
 
 // Kept blocks of one row by one warp for rows too long for the registers: radix select
@@ -939,13 +1048,12 @@ __device__ __forceinline__ void fallback_kept(int m, int nb, int32_t *out, int t
 // ----------------------------------------------------------------------------------
 
 // Work queue order.  Round r (0 <= r < batch + lag_attn) holds, in this order, the score
-// items of sequence r, the select items of sequence r - lag_select, the refine items of
-// sequence r - lag_refine and the attention items of sequence r - lag_attn, each part only
-// when that sequence exists.  Every item still comes after everything it waits for
-// (lag_attn >= lag_refine >= lag_select >= 0), so a CTA that takes items in queue order
+// items of sequence r, the select items of sequence r - lag_select and the attention items
+// of sequence r - lag_attn, each part only when that sequence exists.  Every item still
+// comes after everything it waits for (lag_attn >= lag_select >= 0), so a CTA that takes items in queue order
 // never waits on an item that no CTA has taken; the lags let the score streaming of later
 // sequences overlap the attention of earlier ones.
-enum : int { kItemScore = 0, kItemSelect = 1, kItemRefine = 2, kItemAttn = 3 };
+enum : int { kItemScore = 0, kItemSelect = 1, kItemAttn = 2 };
 struct QueueItem {
   int kind;    // kItem*
   int local;   // index among the items of its kind, in sequence-major order
@@ -954,15 +1062,15 @@ struct QueueItem {
 __device__ __forceinline__ int queue_before(const FusedParams &p, int r) {   // items in rounds < r
   const int B = p.batch;
   const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B;
-  const int ref_per = p.n_refine_items / B, a_per = p.n_attn_items / B;
+  const int a_per = p.n_attn_items / B;
   return s_per * min(max(r, 0), B) + sel_per * min(max(r - p.lag_select, 0), B) +
-         ref_per * min(max(r - p.lag_refine, 0), B) + a_per * min(max(r - p.lag_attn, 0), B);
+         a_per * min(max(r - p.lag_attn, 0), B);
 }
 
 __device__ QueueItem queue_item(const FusedParams &p, int i) {
   const int B = p.batch;
   const int s_per = p.n_score_items / B, sel_per = p.n_select_items / B;
-  const int ref_per = p.n_refine_items / B, a_per = p.n_attn_items / B;
+  const int a_per = p.n_attn_items / B;
   int lo = 0, hi = B + p.lag_attn;   // the last round r in [lo, hi) with queue_before(r) <= i
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -977,11 +1085,6 @@ __device__ QueueItem queue_item(const FusedParams &p, int i) {
   if (ss >= 0 && ss < B) {
     if (off < sel_per) return QueueItem{kItemSelect, ss * sel_per + off};
     off -= sel_per;
-  }
-  const int rs = lo - p.lag_refine;
-  if (rs >= 0 && rs < B) {
-    if (off < ref_per) return QueueItem{kItemRefine, rs * ref_per + off};
-    off -= ref_per;
   }
   return QueueItem{kItemAttn, (lo - p.lag_attn) * a_per + off};
 }
@@ -1005,19 +1108,6 @@ __device__ bool make_desc(const FusedParams &p, QueueItem qi, Desc &d) {
     const int h0 = hr * HS, hs = min(HS, H - h0);
     const int pps = BfTile<D>::kStageBytes / (hs * D * 2);    // pages per stage
     d = Desc{kDescScore, 0, (npg + pps - 1) / pps, b, h0, j0, hs, L};
-    return true;
-  }
-  if (qi.kind == kItemRefine) {
-    // the ambiguous candidates left by the selections of (sequence, rows h0 .. h0 + hs)
-    const int per_seq = (H + kRefineRows - 1) / kRefineRows;
-    const int b = item / per_seq, r = item % per_seq;
-    const int L = __ldg(p.seq_lens + b);
-    if (L < 1 || L > kBlock * p.max_blocks) return false;
-    const int nb = (L + kBlock - 1) / kBlock;
-    if (nb <= p.top_k || p.top_k < 2) return false;             // no selection, or nothing to choose
-    const int h0 = r * kRefineRows;
-    const int hs = min(kRefineRows, H - h0);
-    d = Desc{kDescRefine, 0, 0, b, h0, nb - 1, hs, L};
     return true;
   }
   if (qi.kind == kItemSelect) {
@@ -1067,7 +1157,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
   const bool leader = q == 0;
   const uint64_t policy = l2_policy_evict_first();
   const int H = p.num_kv_heads;
-  const int total = p.n_score_items + p.n_select_items + p.n_refine_items + p.n_attn_items;
+  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
   uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
   uint32_t nd = 0;            // descriptors read (and, by the leader, pushed)
   uint32_t nq = 0;            // leader: score items whose q rows it staged
@@ -1202,109 +1292,6 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
                     p.centroids + (static_cast<int64_t>(pg) * H + h0) * D, row_bytes, &sh.full[s],
                     policy);
         KIN_TOC(kTrPIssue, t_issue);
-      }
-    } else if (d.kind == kDescRefine) {
-      // Rows h0 + hh, hh = q + kProducers k: once a row's selection has released its first
-      // phase, stage its listed ambiguous candidates, kRefinePerStage per ring stage: a
-      // header of (block, first-code score) entries written by the lanes, then the second
-      // centroid code of each candidate's page by a bulk copy.  Then an end marker to each
-      // consumer of this pipeline (the consumers cannot know the stage count).  The
-      // metadata and the first 64 entries of both rows are read at once, then all their
-      // pages, so that the item pays few memory latencies one after the other.
-      const int b = d.row, h0 = d.x0, hs = d.x2;
-      constexpr uint32_t kRowBytes = D * 2;
-      constexpr int kRows = kRefineRows / kProducers;
-      int v[kRows];
-#pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int hh = q + kProducers * k;
-        v[k] = 0;
-        if (lane == 0 && hh < hs) v[k] = wait_flag_value(p.ready + b * H + h0 + hh, 1, sh, p.err);
-        v[k] = __shfl_sync(0xffffffffu, v[k], 0);
-      }
-      __syncwarp();   // the lanes read what the selections released after lane 0's acquire
-      int n_amb[kRows];
-      int2 ent[kRows][2];
-      int pgs[kRows][2];
-#pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int row = b * H + h0 + q + kProducers * k;
-        const bool live = q + kProducers * k < hs && v[k] >= 1 && v[k] < kReadyAll;
-        const int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
-        n_amb[k] = live ? min(__ldcg(&p.amb_meta[row].y), kAmbCapWarp) : 0;
-        ent[k][0] = live ? __ldcg(lst + lane) : make_int2(-1, 0);
-        ent[k][1] = live ? __ldcg(lst + 32 + lane) : make_int2(-1, 0);
-      }
-      const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
-      auto page_of = [&](int j) {
-        if (j < 0 || j >= p.max_blocks) return -1;
-        const int pp = __ldg(trow + j);
-        return pp >= 0 && pp < p.num_pages ? pp : -1;
-      };
-#pragma unroll
-      for (int k = 0; k < kRows; ++k)
-#pragma unroll
-        for (int i = 0; i < 2; ++i) pgs[k][i] = 32 * i + lane < n_amb[k] ? page_of(ent[k][i].x) : -1;
-      int k_item = 0;
-#pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        const int hh = q + kProducers * k;
-        const int row = b * H + h0 + hh;
-        const int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
-        for (int e0 = 0; e0 < n_amb[k]; e0 += kRefinePerStage) {
-          const int cnt = min(kRefinePerStage, n_amb[k] - e0);
-          const int e = e0 + lane;
-          // entry e: held by lane e % 32 in register e / 32 (first 64), else read now
-          const int src = e & 31;
-          const int2 e_lo = make_int2(__shfl_sync(0xffffffffu, ent[k][0].x, src),
-                                      __shfl_sync(0xffffffffu, ent[k][0].y, src));
-          const int2 e_hi = make_int2(__shfl_sync(0xffffffffu, ent[k][1].x, src),
-                                      __shfl_sync(0xffffffffu, ent[k][1].y, src));
-          const int p_lo = __shfl_sync(0xffffffffu, pgs[k][0], src);
-          const int p_hi = __shfl_sync(0xffffffffu, pgs[k][1], src);
-          int2 en = make_int2(-1, 0);
-          int pg = -1;
-          if (lane < cnt) {
-            if (e < 32) {
-              en = e_lo;
-              pg = p_lo;
-            } else if (e < 64) {
-              en = e_hi;
-              pg = p_hi;
-            } else {
-              en = __ldcg(lst + e);
-              pg = page_of(en.x);
-            }
-          }
-          const uint32_t vmask = __ballot_sync(0xffffffffu, pg >= 0);
-          const int cc = k_item % C::kPPC;
-          const uint32_t n = pos[cc];
-          const int s = R::slot(q + kProducers * cc, n);
-          if (lane == 0) wait_bar(&sh.empty[s], R::phase(n) ^ 1u, sh, p.err);
-          __syncwarp();
-          uint8_t *stage = ring + s * R::kStageBytes;
-          if (lane < cnt) reinterpret_cast<int2 *>(stage)[lane] = en;
-          fence_proxy_async_smem();   // later copies into this stage follow these writes
-          __syncwarp();
-          if (lane == 0) {
-            sh.meta[s] = make_int4(hh, e0, cnt, static_cast<int>(vmask));
-            if (vmask != 0)
-              mbar_arrive_expect_tx(&sh.full[s], __popc(vmask) * kRowBytes);
-            else
-              mbar_arrive(&sh.full[s]);
-          }
-          __syncwarp();
-          if (pg >= 0)
-            bulk_load(stage + 256 + lane * kRowBytes,
-                      p.cent_lo + (static_cast<int64_t>(pg) * H + h0 + hh) * D, kRowBytes,
-                      &sh.full[s], policy);
-          ++pos[cc];
-          ++k_item;
-        }
-      }
-      for (int cc = 0; cc < C::kPPC; ++cc) {
-        if (lane == 0) claim(cc, make_int4(-1, 0, 0, 0), 0u);
-        ++pos[cc];
       }
     } else if (d.kind == kDescAttn) {
       // Pages i = q, q + kProducers, ... of the split: lane l reads page
@@ -1441,9 +1428,10 @@ struct QRegs {
 template <int D, int QS>
 __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<D> &qr,
                                               const float *qs, int hs, int nc, uint32_t vmask,
-                                              int lane, float &norm2) {
+                                              int lane, float &hb) {
   constexpr int kPer = D / 32;
   const uint8_t *own = stage + lane * (D * 2);   // centroid `lane`'s row of the stage
+  const float *qown = qs + (lane % hs) * D;       // the group-summed query of its head
   stage += lane * kPer * 2;
   qs += lane * kPer;
   auto unpack = [&](int cc, float (&f)[kPer]) {
@@ -1511,21 +1499,21 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
     }
   }
   const float score = butterfly(v);
-  // lane c: the squared norm of centroid c from its own row, 16-byte chunks in an order
-  // rotated by the lane (rows are 2 D bytes apart, so 8 consecutive lanes read 8 distinct
-  // bank groups)
-  float nrm = 0.f;
+  // lane c: sum_i |qs_i| 2^e(c1_i) of centroid c (row_bound) from its own row, 16-byte
+  // chunks in an order rotated by the lane (rows are 2 D bytes apart, so 8 consecutive
+  // lanes read 8 distinct bank groups)
+  float acc_b = 0.f;
   if (valid(lane)) {
 #pragma unroll 4
     for (int c = 0; c < D / 8; ++c) {
+      const int cr = (c + lane) & (D / 8 - 1);
       float f[8];
-      Elem<__nv_bfloat16>::unpack(
-          *reinterpret_cast<const uint4 *>(own + ((c + lane) & (D / 8 - 1)) * 16), f);
+      Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(own + cr * 16), f);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) nrm = fmaf(f[k], f[k], nrm);
+      for (int k = 0; k < 8; ++k) acc_b += fabsf(qown[8 * cr + k] * pow2_floor(f[k]));
     }
   }
-  norm2 = nrm;
+  hb = acc_b;
   return score;
 }
 
@@ -1563,7 +1551,7 @@ __device__ __forceinline__ void load_qslice(const float *qs, int lane, QSlice<D>
 template <int D>
 __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSlice<D> &qv, int np,
                                                 uint32_t vmask, float *srow_base, int64_t sstride,
-                                                int jst, int lane, float &norm2_max) {
+                                                int jst, int lane, float &hb_max) {
   constexpr int kCh = D / 32;
   const int head = lane >> 2, part = lane & 3, rot = h8_rot<D>(lane);
   const uint8_t *base = stage + head * (D * 2) + part * (D / 4) * 2;
@@ -1582,8 +1570,8 @@ __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSli
       for (int k = 0; k < 8; k += 2) {
         a0 = fmaf(qv.v[c * 8 + k], f[k], a0);
         a1 = fmaf(qv.v[c * 8 + k + 1], f[k + 1], a1);
-        n0 = fmaf(f[k], f[k], n0);
-        n1 = fmaf(f[k + 1], f[k + 1], n1);
+        n0 += fabsf(qv.v[c * 8 + k] * pow2_floor(f[k]));
+        n1 += fabsf(qv.v[c * 8 + k + 1] * pow2_floor(f[k + 1]));
       }
     }
     acc[pp] = a0 + a1;
@@ -1602,21 +1590,25 @@ __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSli
     for (int pp = 0; pp < 4; ++pp) {
       const bool valid = pp < np && ((vmask >> pp) & 1u);
       if (pp < np) __stcg(dst + pp, valid ? acc[pp] : -INFINITY);
-      if (valid) norm2_max = fmaxf(norm2_max, nrm[pp]);
+      if (valid) hb_max = fmaxf(hb_max, nrm[pp]);
     }
   }
 }
 
 // Upper bound of |s - s*| for every candidate of a row, where s is the group score the
 // kernel computes from the first centroid code c1 (bf16) and s* the exact score of the
-// fp32 mean c: |c_i - c1_i| <= 2^-8 |c1_i| (round to nearest, 8 significant bits), so
-// |s - s*| <= 2^-8 sum_i |qs_i| |c1_i| <= 2^-8 |qs|_2 |c1|_2 (Cauchy-Schwarz), plus fp32
-// rounding of the products, sums and of qs itself (below 2^-16 of the same quantity, for
-// d <= 128 and G <= 16).  kBoundScale = 2^-8 + 2^-12 covers both; the 1e-30 term covers
-// subnormal codes, whose error is absolute.
+// fp32 mean c.  c1_i is c_i rounded to nearest with 8 significant bits, so for a normal
+// c1_i in [2^e, 2^(e+1)] the error |c_i - c1_i| is at most half a unit in the last place
+// of c_i's binade, <= 2^(e-8) = 2^-8 pow2_floor(c1_i); hence
+// |s - s*| <= 2^-8 hb with hb = sum_i |qs_i| pow2_floor(c1_i), which the score stage sums
+// per centroid (exact products of powers of two).  fp32 rounding of the score's products
+// and sums, of hb and of qs itself stays below 2^-15 hb for d <= 128 and G <= 16
+// (|c1_i| < 2 pow2_floor(c1_i)).  kBoundScale = 2^-8 + 2^-12 covers both.  A zero or
+// subnormal c1_i (pow2_floor 0) is off by at most 2^-134, which the 1e-30 |qs|_1 term
+// covers.
 constexpr float kBoundScale = 0.00415039062f;   // 2^-8 + 2^-12, exact in fp32
-__device__ __forceinline__ float row_bound(float qn2, float cn2) {
-  return kBoundScale * sqrtf(qn2) * (sqrtf(cn2) + 1e-30f);
+__device__ __forceinline__ float row_bound(float qn1, float hb) {
+  return kBoundScale * hb + 1e-30f * qn1;
 }
 
 // The warp's ring stages of one score item (stages t = q, q + kProducers, ... of the item,
@@ -1634,15 +1626,15 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
   const int b = d.row, h0 = d.x0, hs = d.x2;
   QRegs<D> qr;
   QSlice<D> qv;
-  float qn2 = 0.f;           // |qs|^2 of the lane's head
-  float cn2 = -1.f;          // largest |c1|^2 the lane scored (-1: none)
+  float qn1 = 0.f;           // |qs|_1 of the lane's head
+  float hbm = -1.f;          // largest hb (row_bound) of the centroids the lane scored (-1: none)
   int head;                  // the lane's head within the range
   if constexpr (QS == 8) {
     load_qslice<D>(qs, lane, qv);
 #pragma unroll
-    for (int i = 0; i < D / 4; ++i) qn2 = fmaf(qv.v[i], qv.v[i], qn2);
-    qn2 += __shfl_xor_sync(0xffffffffu, qn2, 1);
-    qn2 += __shfl_xor_sync(0xffffffffu, qn2, 2);
+    for (int i = 0; i < D / 4; ++i) qn1 += fabsf(qv.v[i]);
+    qn1 += __shfl_xor_sync(0xffffffffu, qn1, 1);
+    qn1 += __shfl_xor_sync(0xffffffffu, qn1, 2);
     head = lane >> 2;
   } else {
     if constexpr (QS > 0) {
@@ -1652,7 +1644,7 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
         for (int i = 0; i < D / 32; ++i) qr.v[hh][i] = qs[hh * D + lane * (D / 32) + i];
     }
     head = lane % hs;
-    for (int i = 0; i < D; ++i) qn2 = fmaf(qs[head * D + i], qs[head * D + i], qn2);
+    for (int i = 0; i < D; ++i) qn1 += fabsf(qs[head * D + i]);
   }
   for (int t = q, j = 0; t < d.count; t += kProducers, ++j) {
     if (j % C::kPPC != c) continue;
@@ -1669,16 +1661,16 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
     if constexpr (QS == 8) {
       stage_scores_h8<D>(ring + s * R::kStageBytes, qv, ok ? np : 0, vmask,
                          p.scores + static_cast<int64_t>(b * H + h0) * p.max_blocks, p.max_blocks,
-                         jst, lane, cn2);
+                         jst, lane, hbm);
     } else {
-      float nrm;
-      const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane, nrm);
+      float hb;
+      const float score = stage_scores<D, QS>(ring + s * R::kStageBytes, qr, qs, hs, nc, vmask, lane, hb);
       if (lane < nc) {
         const int pl = lane / hs, hl = lane % hs;
         const bool valid = ((vmask >> pl) & 1u) != 0;
         __stcg(p.scores + static_cast<int64_t>(b * H + h0 + hl) * p.max_blocks + jst + pl,
                valid ? score : -INFINITY);
-        if (valid) cn2 = fmaxf(cn2, nrm);
+        if (valid) hbm = fmaxf(hbm, hb);
       }
     }
     __syncwarp();
@@ -1686,7 +1678,7 @@ __device__ __forceinline__ void score_stages(const FusedParams &p, const Desc &d
     KIN_TOC(kTrCScoreComp, t_sc);
   }
   // bounds are non-negative, so their fp32 bit patterns order like the values
-  if (cn2 >= 0.f) atomicMax(p.bound + b * H + h0 + head, __float_as_uint(row_bound(qn2, cn2)));
+  if (hbm >= 0.f) atomicMax(p.bound + b * H + h0 + head, __float_as_uint(row_bound(qn1, hbm)));
 }
 
 template <int D, int NT>
@@ -1788,13 +1780,21 @@ __device__ __forceinline__ SelScratch sel_scratch(uint8_t *base, bool coop) {
   // cross-warp sums); cooperative: 8 warps x 2 x 16 slots after the histogram
   ss.bal = coop ? reinterpret_cast<uint32_t *>(base + 512 + D * 4 + 1024)
                 : reinterpret_cast<uint32_t *>(base);
+  // ambiguous candidates of the row: one warp: the list after the histogram, pages and
+  // then chosen flags in the histogram area (each dead by the time the next is written);
+  // cooperative: each after the class ballots
+  ss.lst = reinterpret_cast<int2 *>(base + (coop ? 4096 : 2048));
+  ss.pg = coop ? reinterpret_cast<int *>(base + 6144) : ss.hist;
+  ss.lf = coop ? base + 7168 : reinterpret_cast<uint8_t *>(ss.hist);
   return ss;
 }
+static_assert(512 + 128 * 4 + 1024 <= 2048 && 2048 + kAmbCapWarp * 8 <= kSelWarpBytes,
+              "per-warp ambiguous list");
+static_assert(512 + 128 * 4 + 1024 + 8 * 2 * 16 * 4 <= 4096 && 7168 + kAmbCapWarp <= kScratchBytes,
+              "cooperative ambiguous list");
 static_assert(512 + 128 * 4 + 1024 <= kSelWarpBytes, "per-warp selection scratch");
 static_assert(2 * 64 * 4 <= 512, "per-warp class ballots in the xs area");
 static_assert(512 + 128 * 4 + 1024 + 8 * 2 * 16 * 4 <= kScratchBytes, "cooperative selection scratch");
-static_assert(kRefineRows * kAmbCapWarp * 9 + 8 * (kRefineRows / kProducers) * 128 * 4 <= kScratchBytes,
-              "refine item scratch");
 
 template <int D, int NT>
 __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scratch,
@@ -1829,20 +1829,19 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
     const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h0 * G) * D;
     using Bar = typename C::Bar;
     int32_t *ready = p.ready + row;
-    int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
-    int2 *meta = p.amb_meta + row;
+    int2 *lst = ss.lst;
     bool complete = true;
     if (!ok) {
       fallback_kept(m, nb, out, tid, C::kCThreads);
       if (out_user != nullptr) fallback_kept(m, nb, out_user, tid, C::kCThreads);
     } else if (n <= NW * 32 * 2) {
-      complete = cta_select_row<2, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+      complete = cta_select_row<2, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst);
     } else if (n <= NW * 32 * 4) {
-      complete = cta_select_row<4, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+      complete = cta_select_row<4, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst);
     } else if (n <= NW * 32 * 8) {
-      complete = cta_select_row<8, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+      complete = cta_select_row<8, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst);
     } else if (n <= NW * 32 * 16) {
-      complete = cta_select_row<16, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta);
+      complete = cta_select_row<16, NW, D, Bar>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst);
     } else if (warp == 0) {   // longer rows: one warp, radix select over L2
       warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
       __syncwarp();
@@ -1868,18 +1867,17 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
     const float E = __uint_as_float(__ldcg(p.bound + row));
     const RefineCtx rc{p.cent_lo + h * D, trow, static_cast<int64_t>(H) * D, p.num_pages, ss.qs};
     const __nv_bfloat16 *qg = p.q + (static_cast<int64_t>(b) * H * G + h * G) * D;
-    int2 *lst = p.amb_list + static_cast<int64_t>(row) * kAmbCapWarp;
-    int2 *meta = p.amb_meta + row;
+    int2 *lst = ss.lst;
     bool complete = true;
     if (!ok) {
       fallback_kept(m, nb, out, lane, 32);
       if (out_user != nullptr) fallback_kept(m, nb, out_user, lane, 32);
     } else if (n <= 32 * 16) {
-      complete = warp_select_bits<16, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+      complete = warp_select_bits<16, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, lane KIN_TRACE_ARG);
     } else if (n <= 32 * 32) {
-      complete = warp_select_bits<32, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+      complete = warp_select_bits<32, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, lane KIN_TRACE_ARG);
     } else if (n <= 32 * 64) {
-      complete = warp_select_bits<64, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, meta, lane KIN_TRACE_ARG);
+      complete = warp_select_bits<64, D>(srow, n, m, nb, E, rc, qg, G, ss, out, out_user, ready, lst, lane KIN_TRACE_ARG);
     } else {
       warp_select_long<D>(srow, n, m, nb, E, rc, qg, G, ss, out, lane);
       __syncwarp();
@@ -1893,156 +1891,6 @@ __device__ void consume_select(const FusedParams &p, const Desc &d, uint8_t *scr
   KIN_TOC(kTrCSelComp, t_sel);
   C::Bar::sync();   // the scratch is reused by the next item
   if (tid == 0) *reinterpret_cast<volatile int *>(&sh.sel_done) += 1;
-}
-
-// The row's kept list in ascending order into dst[0 .. m): the certain candidates
-// in_list[0 .. n_in) (ascending, global memory) merged with the chosen ambiguous ones
-// ch[0 .. r) (ascending, shared memory); lane l merges the block indices in
-// [l span, (l + 1) span).  Only for the caller's copy of the kept lists.
-__device__ void merge_kept(const int32_t *in_list, int n_in, const int *ch, int r, int nmax,
-                           int32_t *dst, int lane) {
-  const int span = (nmax + 31) / 32;
-  const int v0 = min(nmax, lane * span), v1 = min(nmax, v0 + span);
-  auto lb_in = [&](int v) {
-    int lo = 0, hi = n_in;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (__ldcg(in_list + mid) < v) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-  };
-  auto lb_ch = [&](int v) {
-    int lo = 0, hi = r;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (ch[mid] < v) lo = mid + 1; else hi = mid;
-    }
-    return lo;
-  };
-  int i = lb_in(v0), k = lb_ch(v0);
-  const int i1 = lb_in(v1), k1 = lb_ch(v1);
-  int pos = i + k;
-  while (i < i1 || k < k1) {
-    const int a = i < i1 ? __ldcg(in_list + i) : 0x7fffffff;
-    const int c = k < k1 ? ch[k] : 0x7fffffff;
-    if (a < c) {
-      dst[pos++] = a;
-      ++i;
-    } else {
-      dst[pos++] = c;
-      ++k;
-    }
-  }
-}
-
-// A refine item: the ambiguous candidates that the selections of rows h0 .. h0 + hs - 1
-// left, re-scored with both centroid codes (s + qs . c2), the best m - n_in of them chosen
-// (equal keys to the lower block index) and appended to each row's kept list, which is
-// then released whole.  Consumer warp w takes the stages of its pipeline (rows
-// hh = q, q + kProducers, ...) until its end marker; one warp per row then chooses.
-template <int D, int NT>
-__device__ void consume_refine(const FusedParams &p, const Desc &d, uint8_t *ring, uint8_t *scratch,
-                               FusedShared &sh, uint32_t &n) {
-  using R = Ring<D, NT>;
-  using C = Cfg<D, NT>;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int q = warp % kProducers;
-  const int H = p.num_kv_heads, G = p.group;
-  const int b = d.row, h0 = d.x0, hs = d.x2, nb = d.x1 + 1, m = p.top_k - 1;
-  constexpr int kCap = kAmbCapWarp;
-  uint32_t *lr = reinterpret_cast<uint32_t *>(scratch);                   // [kRefineRows][kCap]
-  int *lj = reinterpret_cast<int *>(scratch + kRefineRows * kCap * 4);     // [kRefineRows][kCap]
-  uint8_t *lf = scratch + kRefineRows * kCap * 8;                          // [kRefineRows][kCap]
-  float *qsw = reinterpret_cast<float *>(scratch + kRefineRows * kCap * 9) +
-               warp * (kRefineRows / kProducers) * D;
-  // the group-summed queries of this warp's rows
-  for (int k = 0, hh = q; hh < hs; ++k, hh += kProducers)
-    group_query<D>(p.q + (static_cast<int64_t>(b) * H * G + (h0 + hh) * G) * D, G, qsw + k * D, lane);
-  __syncwarp();
-  while (true) {
-    const int s = R::slot(warp, n);
-    const bool ok = wait_bar(&sh.full[s], R::phase(n), sh, p.err);
-    ++n;
-    const int4 meta = sh.meta[s];
-    if (!ok || meta.x < 0) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[s]);
-      break;
-    }
-    const int hh = meta.x, e0 = meta.y, cnt = meta.z;
-    const uint32_t vmask = static_cast<uint32_t>(meta.w);
-    const uint8_t *stage = ring + s * R::kStageBytes;
-    if (lane < cnt) {
-      const int2 ent = reinterpret_cast<const int2 *>(stage)[lane];
-      float corr = 0.f;
-      if ((vmask >> lane) & 1u) {
-        // the lane's row is 2 D bytes from its neighbour's: read its 16-byte chunks in an
-        // order rotated by the lane, so that the lanes of a read hit distinct bank groups
-        const float *qs = qsw + (hh / kProducers) * D;
-        const uint4 *c2 = reinterpret_cast<const uint4 *>(stage + 256 + lane * D * 2);
-        constexpr int kCh = D / 8;
-#pragma unroll
-        for (int c = 0; c < kCh; ++c) {
-          const int cr = (c + lane) & (kCh - 1);
-          float f[8];
-          Elem<__nv_bfloat16>::unpack(c2[cr], f);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) corr = fmaf(qs[8 * cr + k], f[k], corr);
-        }
-      }
-      lr[hh * kCap + e0 + lane] = max(score_key(__int_as_float(ent.y) + corr), 2u);
-      lj[hh * kCap + e0 + lane] = ent.x;
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sh.empty[s]);
-  }
-  C::Bar::sync();   // every listed candidate re-scored
-  const unsigned lt = (1u << lane) - 1u;
-  for (int hh = warp; hh < hs; hh += C::kCW) {
-    const int row = b * H + h0 + hh;
-    int v = 0;
-    if (lane == 0) v = ld_acquire_gpu(p.ready + row);
-    v = __shfl_sync(0xffffffffu, v, 0);
-    __syncwarp();
-    if (v < 1 || v >= kReadyAll) continue;
-    const int2 mt = __ldcg(p.amb_meta + row);
-    const int n_in = mt.x, n_amb = min(mt.y, kCap), r = m - n_in;
-    if (n_amb <= r || r <= 0) {   // nothing to choose (not left by a selection): release
-      if (lane == 0) st_release_gpu(p.ready + row, kReadyAll);
-      continue;
-    }
-    if (n_amb <= 64)
-      choose_amb<2>(lr + hh * kCap, n_amb, r, lf + hh * kCap, lane);
-    else
-      choose_amb<kCap / 32>(lr + hh * kCap, n_amb, r, lf + hh * kCap, lane);
-    __syncwarp();
-    // the chosen ones in index order: after the certain ones in the kept list, and
-    // compacted into lr (no longer needed) for the caller's ascending copy
-    int32_t *out = p.sel + static_cast<int64_t>(row) * p.top_k;
-    int *ch = reinterpret_cast<int *>(lr + hh * kCap);
-    int written = 0;
-    for (int e0 = 0; e0 < n_amb; e0 += 32) {
-      const int e = e0 + lane;
-      const bool pick = e < n_amb && lf[hh * kCap + e] != 0;
-      const int j = pick ? lj[hh * kCap + e] : 0;
-      const unsigned km = __ballot_sync(0xffffffffu, pick);
-      const int at = written + __popc(km & lt);
-      __syncwarp();
-      if (pick && at < r) {
-        out[n_in + at] = j;
-        ch[at] = j;
-      }
-      written += __popc(km);
-    }
-    __syncwarp();
-    if (p.sel_out != nullptr) {
-      merge_kept(out, n_in, ch, min(written, r), nb - 1,
-                 p.sel_out + static_cast<int64_t>(row) * p.top_k, lane);
-    }
-    __syncwarp();
-    if (lane == 0) st_release_gpu(p.ready + row, kReadyAll);
-  }
-  C::Bar::sync();   // the scratch is reused by the next item
 }
 
 template <int D, int NT>
@@ -2184,8 +2032,6 @@ __device__ void consumer(const FusedParams &p, uint8_t *ring, uint8_t *scratch,
       KIN_TIC(t0);
       consume_select<D, NT>(p, d, scratch, sh KIN_TRACE_ARG);
       KIN_TOC(kTrCSelect, t0);
-    } else if (d.kind == kDescRefine) {
-      consume_refine<D, NT>(p, d, ring, scratch, sh, n);
     } else if (d.kind == kDescAttn) {
       consume_attention<D, NT>(p, d, ring, scratch, sh, n KIN_TRACE_ARG);
     } else {   // kDescEmptyRow: a sequence whose length is out of range
@@ -2284,7 +2130,7 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
     ctas = sms * (occupancy < 1 ? 1 : occupancy);
     if (dev >= 0 && dev < kMaxDevices) resident[dev].store(ctas, std::memory_order_release);
   }
-  const int total = p.n_score_items + p.n_select_items + p.n_refine_items + p.n_attn_items;
+  const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
   const int grid = min(total, ctas);
   if (grid <= 0) return cudaSuccess;
   fused_decode_kernel<D, NT><<<grid, C::kAllThreads, smem, stream>>>(*kmap, *vmap, p);
@@ -2294,8 +2140,6 @@ cudaError_t launch_d(const FusedParams &p, const CUtensorMap *kmap, const CUtens
 }  // namespace
 
 int fused_max_score_chunk() { return kMaxScoreChunk; }
-int fused_amb_cap() { return kAmbCapWarp; }
-int fused_refine_rows() { return kRefineRows; }
 
 #ifdef KIN_TRACE_CYCLES
 // Copy out (and clear) the cycle counters: [CTA][warp][slot], 160 x 12 x 20 words.

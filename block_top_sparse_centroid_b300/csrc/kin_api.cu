@@ -119,7 +119,7 @@ Counters counter_layout(const kin_decode_args *a, const Plan &pl) {
 }
 
 struct Layout {
-  size_t counters, counter_bytes, part_ml, part_o, scores, sel, amb_list, amb_meta, total;
+  size_t counters, counter_bytes, part_ml, part_o, scores, sel, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -139,13 +139,6 @@ Layout make_layout(const kin_kv_cache *c, const kin_decode_args *a, const Plan &
   if (mode == 0) off = align256(off + sizeof(float) * static_cast<size_t>(pl.rows) * a->max_blocks);
   L.sel = off;
   if (mode == 0) off = align256(off + sizeof(int32_t) * static_cast<size_t>(pl.rows) * a->top_k);
-  L.amb_list = off;
-  L.amb_meta = off;
-  if (mode == 0 && c->dtype == KIN_BF16) {
-    off = align256(off + sizeof(int2) * static_cast<size_t>(pl.rows) * fused_amb_cap());
-    L.amb_meta = off;
-    off = align256(off + sizeof(int2) * static_cast<size_t>(pl.rows));
-  }
   L.total = off;
   return L;
 }
@@ -375,8 +368,6 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.attn_cnt = cnt + ck.attn_cnt;
     fp.ready = cnt + ck.ready;
     fp.bound = reinterpret_cast<uint32_t *>(cnt + ck.bound);
-    fp.amb_list = reinterpret_cast<int2 *>(ws + L.amb_list);
-    fp.amb_meta = reinterpret_cast<int2 *>(ws + L.amb_meta);
     fp.exit_cnt = cnt + ck.exit_cnt;
     fp.counters = cnt;
     fp.n_counters = static_cast<int>(ck.count);
@@ -403,9 +394,6 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     // 256 rows 5 % slower).
     fp.coop_select = pl.rows <= kPlanSMs ? 1 : 0;
     fp.n_select_items = mode == 0 ? a->batch * (fp.coop_select ? c->num_kv_heads : pl.head_ranges) : 0;
-    // refine items: groups of fused_refine_rows() rows of a sequence
-    const int rr = fused_refine_rows();
-    fp.n_refine_items = mode == 0 ? a->batch * ((c->num_kv_heads + rr - 1) / rr) : 0;
     fp.n_attn_items = pl.rows * pl.max_splits;
     // Queue lags in rounds (one sequence per round).  At the start every CTA takes an item
     // and prefetches the next, so the first two waves of the queue (2 x 148 items) start
@@ -417,19 +405,16 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
       const int span = 2 * kPlanSMs;
       fp.lag_select = s_per > 0 ? (span + s_per - 1) / s_per : 0;
       fp.lag_attn = fp.lag_select + (span + s_per + sel_per - 1) / (s_per + sel_per);
-      // a refine item waits for its selection's first phase: half-way between the two
-      fp.lag_refine = fp.lag_select + (fp.lag_attn - fp.lag_select + 1) / 2;
       if (fp.coop_select) {
         // No more rows than CTAs: every row's selection runs on a CTA of its own anyway, so
-        // the queue takes all score items, then all select items, then all refine items,
-        // then all attention items (measured: 16 sequences of 8K-32K tokens 12 % faster
-        // than interleaved, 8 sequences 6 %).
+        // the queue takes all score items, then all select items, then all attention items
+        // (measured: 16 sequences of 8K-32K tokens 12 % faster than interleaved, 8
+        // sequences 6 %).
         fp.lag_select = a->batch;
-        fp.lag_refine = 2 * a->batch;
-        fp.lag_attn = 3 * a->batch;
+        fp.lag_attn = 2 * a->batch;
       }
     } else {
-      fp.lag_select = fp.lag_refine = fp.lag_attn = 0;
+      fp.lag_select = fp.lag_attn = 0;
     }
 
     fp.append_final = append;

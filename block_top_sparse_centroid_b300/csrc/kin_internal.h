@@ -82,9 +82,6 @@ struct FusedParams {
   int32_t *attn_cnt;               // [B*H] split arrivals
   int32_t *ready;                  // [B*H] selection published
   uint32_t *bound;                 // [B*H] score error bound of the row (fp32 bits, max)
-  int2 *amb_list;                  // [B*H, fused_amb_cap()] ambiguous candidates a selection
-                                   //   leaves to a refine item: {block j, first-code score bits}
-  int2 *amb_meta;                  // [B*H] {candidates kept for certain, ambiguous ones listed}
   int32_t *exit_cnt;               // CTAs finished (self_clean only)
   int32_t *counters;               // all of the above counters, n_counters words
   int n_counters;
@@ -96,12 +93,11 @@ struct FusedParams {
   int heads_per_range, head_ranges;  // HS = min(H, 32) heads per score / select item
   int score_chunk, chunks_per_seq;   // candidate blocks per score item, items per range
   int items_per_split, splits_per_row;
-  int n_score_items, n_select_items, n_refine_items, n_attn_items;
+  int n_score_items, n_select_items, n_attn_items;
   // Queue order: round r holds the score items of sequence r, the select items of
-  // sequence r - lag_select, the refine items of sequence r - lag_refine and the attention
-  // items of sequence r - lag_attn (each part only when that sequence exists), so that
-  // streaming scores and attention overlap.
-  int lag_select, lag_refine, lag_attn;
+  // sequence r - lag_select and the attention items of sequence r - lag_attn (each part
+  // only when that sequence exists), so that streaming scores and attention overlap.
+  int lag_select, lag_attn;
   int coop_select;                 // select items are single rows, selected by all consumer warps
   int append_final;
   float sm_scale;
@@ -110,11 +106,6 @@ cudaError_t launch_fused(int head_dim, const FusedParams &p, const CUtensorMap *
                          const CUtensorMap *vmap, cudaStream_t stream);
 // Largest score chunk the fused kernel accepts (candidate blocks per score item).
 int fused_max_score_chunk();
-// Ambiguous candidates one row's selection can leave to a refine item (longer lists are
-// settled by the selection itself).
-int fused_amb_cap();
-// Rows of a sequence per refine item.
-int fused_refine_rows();
 
 // Tiling facts the host needs for workspace sizing and split planning.
 int attention_warps();
