@@ -51,6 +51,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-token", action="store_true",
+                    help="skip the token-level (oracle) top-k decode of the same step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-others", action="store_true",
                     help="skip the single-step Qwen3 workloads reported under \"configs\"")
@@ -503,7 +505,7 @@ def timed_graphs(cx, step_fns, n_warm: int, n_steps: int):
         cx.flush.zero_()
         graphs[i % n].replay()
     cx.barrier()
-    res = dict(step_ms=[], kern_ms=[], write_ms=[], idx=[])
+    res = dict(step_ms=[], kern_ms=[], write_ms=[], phase_ms=[], idx=[])
     for i in range(n_steps):
         j = i % n
         cx.flush.zero_()                         # L2 flush, outside the timed events
@@ -513,6 +515,7 @@ def timed_graphs(cx, step_fns, n_warm: int, n_steps: int):
         res["step_ms"].append(e[0].elapsed_time(e[3]))
         res["kern_ms"].append(e[2].elapsed_time(e[3]))
         res["write_ms"].append(e[4].elapsed_time(e[5]))
+        res["phase_ms"].append([e[k].elapsed_time(e[k + 1]) for k in range(3)])
         res["idx"].append(j)
     cx.barrier()
     return res
@@ -548,6 +551,54 @@ def run_single(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=Non
     if want_e2e:
         r["e2e"] = e2e_single(cx, dw, n_warm, n_steps)
     return r, dw
+
+
+def token_bytes(cfg, lens, budget: int) -> dict:
+    """Algorithmic bytes of one token top-k step (every key read once to score it, the kept
+    tokens' keys and values read again to attend, q and out) and of its score kernel alone
+    (the keys, q, and one fp32 score written per token)."""
+    H, d, G = cfg.num_kv_heads, cfg.head_dim, cfg.group
+    es = 2 if cfg.dtype == "bf16" else 4
+    ntok = sum(lens)
+    all_k = ntok * H * d * es
+    kept = sum(min(L, budget) for L in lens) * H * 2 * d * es
+    qo = 2 * len(lens) * H * G * d * es
+    return {"step": all_k + kept + qo, "score_kernel": all_k + len(lens) * H * G * d * es + ntok * H * 4,
+            "all_k": all_k, "kept_kv": kept, "qo": qo}
+
+
+def run_token(cx, cfg, dw, n_warm, n_steps) -> dict:
+    """The token-level (oracle) top-k decode of the same step (budget: 16 tokens per kept
+    block, the equal-KV budget), timed like the block decode: score, select and attend
+    kernel times, the step rate, and the score kernel's roofline (it streams every key)."""
+    import torch
+    import block_top_sparse_centroid_b300 as K
+    budget = 16 * cfg.top_k
+    ws = K.Workspace(cx.dev)
+
+    def step(evs):
+        evs[4].record()
+        evs[5].record()
+        K.token_topk_decode(dw.cache, dw.q, dw.table, dw.seq0, budget, cfg.sm_scale, out=dw.out,
+                            workspace=ws, err_flag=dw.err, events=evs[:4])
+
+    sp = timed_graphs(cx, [step], n_warm, n_steps)
+    torch.cuda.synchronize()
+    if int(dw.err.item()) != 0:
+        raise RuntimeError(f"device error flag {int(dw.err.item())}")
+    byt = token_bytes(cfg, dw.lens0, budget)
+    step_s = cx.job_seconds(sp["step_ms"])
+    ph = [sum(x[k] for x in sp["phase_ms"]) / len(sp["phase_ms"]) for k in range(3)]
+    score_gbs = byt["score_kernel"] / (ph[0] / 1e3) / 1e9
+    return {"budget_tokens": budget, "value": whole_job_rate(cfg.batch, cx.world, step_s),
+            "unit": UNIT, "ms_per_step": step_s * 1e3,
+            "score_us": ph[0] * 1e3, "select_us": ph[1] * 1e3, "attend_us": ph[2] * 1e3,
+            "bytes_per_step": byt["step"],
+            "step_gbs": byt["step"] / step_s / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "token_score_kernel", "achieved": score_gbs,
+                         "peak": cx.peak, "unit": "GB/s", "frac": score_gbs / cx.peak,
+                         "bytes_per_launch": byt["score_kernel"], "launch_us": ph[0] * 1e3},
+            "launches": 3 * len(sp["idx"])}
 
 
 def summarize(cx, cfg, sp, step_bytes, de, dense_bytes) -> dict:
@@ -782,6 +833,12 @@ def main() -> int:
     runner = run_loop if loop else run_single
     r, dw = runner(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e, inp)
     trec = traffic_record(describe(cfg))
+    tok = None
+    if cfg.dtype == "bf16" and not args.no_token:
+        # the decode's initial state (positions below the initial lengths are untouched by
+        # the loop's token writes)
+        tok = run_token(cx, cfg, dw, 5, min(args.steps, args.other_steps))
+        r["launches"] += tok["launches"]
     del dw
     torch.cuda.empty_cache()
 
@@ -790,6 +847,9 @@ def main() -> int:
         for i in (1, 2, 3):
             oc = replica_config(W.CONFIGS[i], cx.rank)
             o, odw = run_single(cx, oc, 5, args.other_steps, not args.no_dense, False)
+            otok = None if args.no_token else run_token(cx, oc, odw, 5, args.other_steps)
+            if otok is not None:
+                r["launches"] += otok["launches"]
             del odw
             torch.cuda.empty_cache()
             orec = traffic_record(describe(oc))
@@ -801,7 +861,7 @@ def main() -> int:
                              "traffic": orec["dram_bytes_per_launch"] if orec else None,
                              "bytes_per_launch": o["bytes_per_step"],
                              "launch_us": o["kernel_us"]},
-                "dense": o.get("dense"), "clocks": o["clocks"]}
+                "dense": o.get("dense"), "clocks": o["clocks"], "token_topk": otok}
             r["launches"] += o["launches"]
 
     per_launch_kernel = "fused_decode_kernel" if cfg.dtype == "bf16" else "attn_f32_kernel"
@@ -835,6 +895,7 @@ def main() -> int:
         "clocks": r["clocks"],
         "e2e": r.get("e2e"),
         "dense": r.get("dense"),
+        "token_topk": tok,
     }
     if loop:
         line["roofline"]["unique_step0"] = r["unique"]

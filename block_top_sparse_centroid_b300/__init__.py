@@ -9,9 +9,10 @@ from . import _lib
 from ._lib import KinError, load as load_library
 from .api import (BLOCK, PagedKVCache, PreparedDecode, Workspace, blocktopk_decode,
                   centroids_append, centroids_build, decode_timed, dense_decode,
-                  prepare_blocktopk_decode, prepare_dense_decode, workspace_size)
+                  prepare_blocktopk_decode, prepare_dense_decode, prepare_token_topk_decode,
+                  token_topk_decode, workspace_size)
 
 __all__ = ["BLOCK", "KinError", "PagedKVCache", "PreparedDecode", "Workspace",
            "blocktopk_decode", "centroids_append", "centroids_build", "decode_timed",
            "dense_decode", "prepare_blocktopk_decode", "prepare_dense_decode",
-           "workspace_size", "load_library"]
+           "prepare_token_topk_decode", "token_topk_decode", "workspace_size", "load_library"]

@@ -28,6 +28,7 @@ KIN_DECODE_APPEND_FINAL = 1
 
 MODE_BLOCKTOPK = 0
 MODE_DENSE = 1
+MODE_TOKENTOPK = 2
 
 
 class KvCache(ctypes.Structure):
@@ -59,6 +60,7 @@ SIGNATURES = {
                                      c_void_p]),
     "kin_blocktopk_decode": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
     "kin_dense_decode": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
+    "kin_token_topk_decode": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
     "kin_blocktopk_decode_static": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_void_p]),
     "kin_decode_timed": (c_int, [POINTER(KvCache), POINTER(DecodeArgs), c_int32,
                                  POINTER(c_void_p), c_void_p]),

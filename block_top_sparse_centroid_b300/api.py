@@ -104,14 +104,15 @@ def _shape_args(cache: PagedKVCache, batch: int, num_q_heads: int, max_blocks: i
 
 
 def workspace_size(cache: PagedKVCache, batch: int, num_q_heads: int, max_blocks: int,
-                   top_k: int = 1, dense: bool = False) -> int:
-    """Bytes of workspace one decode call needs (kin_workspace_size)."""
+                   top_k: int = 1, dense: bool = False, tokens: bool = False) -> int:
+    """Bytes of workspace one decode call needs (kin_workspace_size): block top-k, dense
+    (dense=True) or token top-k (tokens=True, top_k in tokens)."""
     lib = L.load()
     c = cache.c_struct()
     a = _shape_args(cache, batch, num_q_heads, max_blocks, top_k)
     n = ctypes.c_size_t(0)
-    L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a),
-                                   L.MODE_DENSE if dense else L.MODE_BLOCKTOPK, ctypes.byref(n)),
+    mode = L.MODE_TOKENTOPK if tokens else (L.MODE_DENSE if dense else L.MODE_BLOCKTOPK)
+    L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a), mode, ctypes.byref(n)),
             "kin_workspace_size")
     return int(n.value)
 
@@ -190,8 +191,8 @@ def centroids_append(cache: PagedKVCache, page_ids: torch.Tensor, centroids: tor
 
 class PreparedDecode:
     """A decode call whose tensors are fixed: shapes, dtypes and devices are checked and the
-    C structs built once, so that each call only enqueues the kernels (kin_blocktopk_decode
-    or kin_dense_decode).  It keeps every tensor it was given alive.  For a decode loop whose
+    C structs built once, so that each call only enqueues the kernels (kin_blocktopk_decode,
+    kin_dense_decode or kin_token_topk_decode).  It keeps every tensor it was given alive.  For a decode loop whose
     buffers stay the same from step to step (q, out, the cache, the block table and
     seq_lens updated in place), this is the low-overhead way to call the library.
 
@@ -228,6 +229,11 @@ class PreparedDecode:
                 _need(sel_blocks, "sel_blocks", (B, H, top_k), torch.int32, dev)
             if scores is not None:
                 _need(scores, "scores", (B, H, maxb), torch.float32, dev)
+        if mode == L.MODE_TOKENTOPK:
+            if sel_blocks is not None:
+                _need(sel_blocks, "sel_tokens", (B, H, top_k), torch.int32, dev)
+            if scores is not None:
+                _need(scores, "scores", (B, H, 16 * maxb), torch.float32, dev)
         a = L.DecodeArgs()
         a.batch, a.num_q_heads, a.max_blocks, a.top_k = B, Hq, maxb, int(top_k)
         a.sm_scale = float(sm_scale)
@@ -237,8 +243,8 @@ class PreparedDecode:
         a.flags = L.KIN_DECODE_APPEND_FINAL if append_final else 0
         a.out = out.data_ptr()
         a.lse = None if lse is None else lse.data_ptr()
-        a.sel_blocks = None if (sel_blocks is None or mode != L.MODE_BLOCKTOPK) else sel_blocks.data_ptr()
-        a.scores = None if (scores is None or mode != L.MODE_BLOCKTOPK) else scores.data_ptr()
+        a.sel_blocks = None if (sel_blocks is None or mode == L.MODE_DENSE) else sel_blocks.data_ptr()
+        a.scores = None if (scores is None or mode == L.MODE_DENSE) else scores.data_ptr()
         c = cache.c_struct()
         need = ctypes.c_size_t(0)
         L.check(lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(a), mode, ctypes.byref(need)),
@@ -250,8 +256,9 @@ class PreparedDecode:
                       ws, err_flag)
         self._lib, self._c, self._a, self._mode, self._dev = lib, c, a, mode, dev
         self._cref, self._aref = ctypes.byref(c), ctypes.byref(a)
-        self._fn = lib.kin_blocktopk_decode if mode == L.MODE_BLOCKTOPK else lib.kin_dense_decode
-        self._name = "kin_blocktopk_decode" if mode == L.MODE_BLOCKTOPK else "kin_dense_decode"
+        self._name = {L.MODE_BLOCKTOPK: "kin_blocktopk_decode", L.MODE_DENSE: "kin_dense_decode",
+                      L.MODE_TOKENTOPK: "kin_token_topk_decode"}[mode]
+        self._fn = getattr(lib, self._name)
         self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
         self.out = out
 
@@ -302,6 +309,41 @@ def prepare_dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torc
     """A dense decode call (kin_dense_decode) prepared once, run by calling it."""
     return PreparedDecode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, None,
                           out, lse, None, None, workspace, err_flag, False, stream)
+
+
+def prepare_token_topk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                              seq_lens: torch.Tensor, top_tokens: int, sm_scale: float,
+                              out: Optional[torch.Tensor] = None,
+                              lse: Optional[torch.Tensor] = None,
+                              sel_tokens: Optional[torch.Tensor] = None,
+                              scores: Optional[torch.Tensor] = None,
+                              workspace: Optional[Workspace] = None,
+                              err_flag: Optional[torch.Tensor] = None,
+                              stream=None) -> PreparedDecode:
+    """A token top-k decode call (kin_token_topk_decode) prepared once, run by calling it."""
+    return PreparedDecode(L.MODE_TOKENTOPK, cache, q, block_table, seq_lens, sm_scale,
+                          top_tokens, None, out, lse, sel_tokens, scores, workspace, err_flag,
+                          False, stream)
+
+
+def token_topk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
+                      seq_lens: torch.Tensor, top_tokens: int, sm_scale: float,
+                      out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                      sel_tokens: Optional[torch.Tensor] = None,
+                      scores: Optional[torch.Tensor] = None,
+                      workspace: Optional[Workspace] = None,
+                      err_flag: Optional[torch.Tensor] = None, stream=None,
+                      events=None) -> torch.Tensor:
+    """One token-level (oracle) top-k decode step: every token scored by the group-summed
+    q.k, the top_tokens best of each (sequence, KV head) kept, attention over them
+    (kin_token_topk_decode; with events, kin_decode_timed mode 2).  sel_tokens: optional
+    [B, H, top_tokens] int32 kept positions; scores: optional [B, H, 16 max_blocks] fp32."""
+    call = PreparedDecode(L.MODE_TOKENTOPK, cache, q, block_table, seq_lens, sm_scale,
+                          top_tokens, None, out, lse, sel_tokens, scores, workspace, err_flag,
+                          False)
+    if events is not None:
+        return call.timed(list(events), stream)
+    return call(stream)
 
 
 def _event_handle(ev: "torch.cuda.Event", stream, dev) -> int:

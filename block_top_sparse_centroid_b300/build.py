@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libkin.so")
 VARIANTS = {"shortwait": ["-DKIN_MAX_WAIT_TRIES=4096u"]}
 
-SOURCES = ["centroid.cu", "score_select.cu", "attention.cu", "decode_fused.cu", "kin_api.cu",
-           "noalloc.cu"]
+SOURCES = ["centroid.cu", "score_select.cu", "attention.cu", "decode_fused.cu", "token_topk.cu",
+           "kin_api.cu", "noalloc.cu"]
 HEADERS = ["kin_common.cuh", "attn_common.cuh", "kin_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -180,7 +180,13 @@ kin_status check_args(const kin_kv_cache *c, const kin_decode_args *a, int mode)
   if (G > 16) return fail(KIN_ERR_UNSUPPORTED, "group size %d > 16", G);
   if (a->max_blocks < 1 || a->max_blocks > kMaxBlocksLimit)
     return fail(KIN_ERR_UNSUPPORTED, "max_blocks %d outside 1..%d", a->max_blocks, kMaxBlocksLimit);
-  if (mode == 0 && a->top_k < 1) return fail(KIN_ERR_INVALID_ARG, "top_k %d < 1", a->top_k);
+  if ((mode == 0 || mode == 2) && a->top_k < 1)
+    return fail(KIN_ERR_INVALID_ARG, "top_k %d < 1", a->top_k);
+  if (mode == 2 && c->dtype != KIN_BF16)
+    return fail(KIN_ERR_UNSUPPORTED, "token top-k decode needs a bf16 cache");
+  if (mode == 2 && a->flags != 0)
+    return fail(KIN_ERR_INVALID_ARG, "token top-k decode takes no flags (0x%x)",
+                static_cast<unsigned>(a->flags));
   if (!(a->sm_scale > 0.f) || a->sm_scale == INFINITY)
     return fail(KIN_ERR_INVALID_ARG, "sm_scale must be a positive finite number");
   if (a->q == nullptr || a->block_table == nullptr || a->seq_lens == nullptr || a->out == nullptr)
@@ -303,6 +309,111 @@ kin_status record(void *const *events, int i, cudaStream_t stream) {
           : cudaEventRecord(ev, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
   return KIN_OK;
+}
+
+// Token top-k: attention CTAs per row (splits) so that about three per SM run at once,
+// each taking a multiple of one pass of its warps' 16-token tiles.
+struct TokenPlan {
+  int rows, group, keep_max, tokens_per_split, splits;
+};
+
+TokenPlan make_token_plan(const kin_kv_cache *c, const kin_decode_args *a) {
+  TokenPlan tp{};
+  tp.rows = a->batch * c->num_kv_heads;
+  tp.group = a->num_q_heads / c->num_kv_heads;
+  const long long cap = static_cast<long long>(kBlock) * a->max_blocks;
+  tp.keep_max = static_cast<int>(a->top_k < cap ? a->top_k : cap);
+  const int tile = token_tile_tokens();
+  const int max_useful = (tp.keep_max + tile - 1) / tile;
+  int splits = (3 * kPlanSMs + tp.rows - 1) / tp.rows;
+  if (splits > max_useful) splits = max_useful;
+  if (splits < 1) splits = 1;
+  int tps = (tp.keep_max + splits - 1) / splits;
+  tps = (tps + tile - 1) / tile * tile;
+  tp.tokens_per_split = tps;
+  tp.splits = (tp.keep_max + tps - 1) / tps;
+  return tp;
+}
+
+struct TokenLayout {
+  size_t counters, part_ml, part_o, scores, gather, total;
+};
+
+TokenLayout make_token_layout(const kin_kv_cache *c, const kin_decode_args *a, const TokenPlan &tp) {
+  TokenLayout L{};
+  size_t off = 0;
+  L.counters = off;
+  off = align256(off + sizeof(int32_t) * static_cast<size_t>(tp.rows));
+  L.part_ml = off;
+  off = align256(off + sizeof(float) * 2 * static_cast<size_t>(tp.rows) * tp.splits * tp.group);
+  L.part_o = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(tp.rows) * tp.splits * tp.group *
+                           c->head_dim);
+  L.scores = off;
+  off = align256(off + sizeof(float) * static_cast<size_t>(tp.rows) * kBlock * a->max_blocks);
+  L.gather = off;
+  off = align256(off + sizeof(int32_t) * static_cast<size_t>(tp.rows) * a->top_k);
+  L.total = off;
+  return L;
+}
+
+kin_status run_token_decode(const kin_kv_cache *c, const kin_decode_args *a, cudaStream_t stream,
+                            void *const *events = nullptr) {
+  kin_status s = check_cache(c);
+  if (s != KIN_OK) return s;
+  s = check_args(c, a, 2);
+  if (s != KIN_OK) return s;
+  const TokenPlan tp = make_token_plan(c, a);
+  const TokenLayout L = make_token_layout(c, a, tp);
+  if (a->workspace == nullptr)
+    return fail(KIN_ERR_WORKSPACE, "workspace is NULL (need %zu bytes)", L.total);
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0)
+    return fail(KIN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (a->workspace_bytes < L.total)
+    return fail(KIN_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", a->workspace_bytes, L.total);
+  if (events != nullptr && (events[0] == nullptr || events[1] == nullptr ||
+                            events[2] == nullptr || events[3] == nullptr))
+    return fail(KIN_ERR_INVALID_ARG, "events must hold 4 created CUDA events");
+  DeviceScope scope;
+  s = scope.enter(c->k_pages);
+  if (s != KIN_OK) return s;
+  uint8_t *ws = static_cast<uint8_t *>(a->workspace);
+  TokenParams p{};
+  p.q = static_cast<const __nv_bfloat16 *>(a->q);
+  p.k_pages = static_cast<const __nv_bfloat16 *>(c->k_pages);
+  p.v_pages = static_cast<const __nv_bfloat16 *>(c->v_pages);
+  p.block_table = a->block_table;
+  p.seq_lens = a->seq_lens;
+  p.out = a->out;
+  p.lse = a->lse;
+  p.scores = a->scores != nullptr ? a->scores : reinterpret_cast<float *>(ws + L.scores);
+  p.score_stride = static_cast<int64_t>(kBlock) * a->max_blocks;
+  p.gather = reinterpret_cast<int32_t *>(ws + L.gather);
+  p.sel_out = a->sel_blocks;
+  p.part_o = reinterpret_cast<float *>(ws + L.part_o);
+  p.part_ml = reinterpret_cast<float *>(ws + L.part_ml);
+  p.counters = reinterpret_cast<int32_t *>(ws + L.counters);
+  p.err = a->err_flag;
+  p.num_pages = c->num_pages;
+  p.batch = a->batch;
+  p.num_kv_heads = c->num_kv_heads;
+  p.group = tp.group;
+  p.max_blocks = a->max_blocks;
+  p.top_k = a->top_k;
+  p.splits = tp.splits;
+  p.tokens_per_split = tp.tokens_per_split;
+  p.sm_scale = a->sm_scale;
+  if ((s = record(events, 0, stream)) != KIN_OK) return s;
+  cudaError_t e = launch_token_score(c->head_dim, p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "token score kernel launch");
+  if ((s = record(events, 1, stream)) != KIN_OK) return s;
+  e = launch_token_select(p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "token select kernel launch");
+  if ((s = record(events, 2, stream)) != KIN_OK) return s;
+  e = launch_token_attn(c->head_dim, p, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "token attention kernel launch");
+  if ((s = record(events, 3, stream)) != KIN_OK) return s;
+  return ok();
 }
 
 kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
@@ -542,14 +653,18 @@ kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *
                               size_t *bytes) {
   using namespace kin;
   if (bytes == nullptr) return fail(KIN_ERR_INVALID_ARG, "bytes is NULL");
-  if (mode != 0 && mode != 1) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0 or 1", mode);
+  if (mode < 0 || mode > 2) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0, 1 or 2", mode);
   kin_status s = check_cache_shape(cache);
   if (s != KIN_OK) return s;
   if (args == nullptr) return fail(KIN_ERR_INVALID_ARG, "args is NULL");
   if (args->batch < 1 || args->num_q_heads < 1 || args->max_blocks < 1 ||
       args->max_blocks > kMaxBlocksLimit || args->num_q_heads % cache->num_kv_heads != 0 ||
-      args->num_q_heads / cache->num_kv_heads > 16 || (mode == 0 && args->top_k < 1))
+      args->num_q_heads / cache->num_kv_heads > 16 || (mode != 1 && args->top_k < 1))
     return fail(KIN_ERR_INVALID_ARG, "bad shapes for workspace sizing");
+  if (mode == 2) {
+    *bytes = make_token_layout(cache, args, make_token_plan(cache, args)).total;
+    return ok();
+  }
   const Plan pl = make_plan(cache, args, mode);
   *bytes = make_layout(cache, args, pl, mode).total;
   return ok();
@@ -579,11 +694,17 @@ kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_args *ar
   return kin::run_decode(cache, args, 1, reinterpret_cast<cudaStream_t>(stream));
 }
 
+kin_status kin_token_topk_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                                 kin_stream_t stream) {
+  return kin::run_token_decode(cache, args, reinterpret_cast<cudaStream_t>(stream));
+}
+
 kin_status kin_decode_timed(const kin_kv_cache *cache, const kin_decode_args *args, int32_t mode,
                             void *const *events, kin_stream_t stream) {
   using namespace kin;
-  if (mode != 0 && mode != 1) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0 or 1", mode);
+  if (mode < 0 || mode > 2) return fail(KIN_ERR_INVALID_ARG, "mode %d is not 0, 1 or 2", mode);
   if (events == nullptr) return fail(KIN_ERR_INVALID_ARG, "events is NULL");
+  if (mode == 2) return kin::run_token_decode(cache, args, reinterpret_cast<cudaStream_t>(stream), events);
   return kin::run_decode(cache, args, mode, reinterpret_cast<cudaStream_t>(stream), events);
 }
 

@@ -102,6 +102,35 @@ struct FusedParams {
   int append_final;
   float sm_scale;
 };
+// Token-level top-k decode (bf16 caches): score every token, select the top_k per row,
+// attend over the kept tokens (token_topk.cu).
+struct TokenParams {
+  const __nv_bfloat16 *q;          // [B, H*G, d]
+  const __nv_bfloat16 *k_pages;    // [P, H, 16, d]
+  const __nv_bfloat16 *v_pages;
+  const int32_t *block_table;      // [B, max_blocks]
+  const int32_t *seq_lens;         // [B]
+  void *out;                       // [B, H*G, d]
+  float *lse;                      // [B, H*G] or NULL
+  float *scores;                   // [B*H, score_stride] token scores
+  int64_t score_stride;            // 16 * max_blocks
+  int32_t *gather;                 // [B*H, top_k] kept tokens' rows of the [P*H*16, d] view
+  int32_t *sel_out;                // [B*H, top_k] kept positions ascending, or NULL
+  float *part_o, *part_ml;         // split partials [B*H, splits, G, d] and [.., G, 2]
+  int32_t *counters;               // [B*H] split arrivals (zero between calls)
+  int32_t *err;
+  int64_t num_pages;
+  int batch, num_kv_heads, group, max_blocks;
+  int top_k;                       // tokens kept per row
+  int splits, tokens_per_split;    // attention CTAs per row and kept tokens each
+  float sm_scale;
+};
+cudaError_t launch_token_score(int head_dim, const TokenParams &p, cudaStream_t stream);
+cudaError_t launch_token_select(const TokenParams &p, cudaStream_t stream);
+cudaError_t launch_token_attn(int head_dim, const TokenParams &p, cudaStream_t stream);
+// Kept tokens one attention CTA takes per pass (its warps' tiles); splits are multiples.
+int token_tile_tokens();
+
 cudaError_t launch_fused(int head_dim, const FusedParams &p, const CUtensorMap *kmap,
                          const CUtensorMap *vmap, cudaStream_t stream);
 // Largest score chunk the fused kernel accepts (candidate blocks per score item).

@@ -136,10 +136,9 @@ KIN_API const char *kin_status_str(kin_status s);
 /* One-line description of the last failed call on this host thread ("" if none). */
 KIN_API const char *kin_last_error(void);
 
-/* Bytes of workspace that kin_blocktopk_decode / kin_dense_decode need for these
- * shapes (pointers inside the structs are not read).  The dense and the block top-k
- * call may share one workspace sized for the larger of the two (mode 0 = block top-k,
- * mode 1 = dense). */
+/* Bytes of workspace that kin_blocktopk_decode (mode 0), kin_dense_decode (mode 1) or
+ * kin_token_topk_decode (mode 2) needs for these shapes (pointers inside the structs are
+ * not read).  Calls of different modes may share one workspace sized for the largest. */
 KIN_API kin_status kin_workspace_size(const kin_kv_cache *cache, const kin_decode_args *args,
                               int32_t mode, size_t *bytes);
 
@@ -189,6 +188,24 @@ KIN_API kin_status kin_blocktopk_decode(const kin_kv_cache *cache, const kin_dec
 KIN_API kin_status kin_dense_decode(const kin_kv_cache *cache, const kin_decode_args *args,
                             kin_stream_t stream);
 
+/* One token-level ("oracle") top-k decode step, the exact-selection upper bound that
+ * block top-k approximates (scime summary of "Kinetics: Rethinking Test-Time Scaling
+ * Laws", "Key results"; Pith review of the paper, "assumptions").  For every sequence b
+ * and KV head h with L = seq_lens[b] tokens and B = args->top_k (tokens, not blocks):
+ *   score   s_t = sum_g q[b, hG+g, :] . K[t, h, :]  for every t < L  (fp32)
+ *   select  T = the B largest s_t, ties to the lower position; every token if L <= B
+ *   attend  out[b, hG+g, :] = softmax over T of sm_scale * q.k, applied to V
+ * No token is forced in.  Reads every key of every row once (three kernels: score,
+ * select, attend).  bf16 caches only (KIN_ERR_UNSUPPORTED otherwise); args->flags must be
+ * 0 and args->centroids is not read.  args->sel_blocks, optional, is [B, H, top_k]: the
+ * kept token positions ascending, -1 padded when L < top_k.  args->scores, optional, is
+ * [B, H, 16 * max_blocks]: s_t of positions t < L (other entries untouched).  The
+ * workspace (kin_workspace_size mode 2) follows the rules of kin_decode_args.workspace;
+ * kin_decode_timed mode 2 records events[1] after scoring and events[2] after
+ * selection. */
+KIN_API kin_status kin_token_topk_decode(const kin_kv_cache *cache, const kin_decode_args *args,
+                                         kin_stream_t stream);
+
 /* kin_blocktopk_decode for callers that cannot allocate device memory -- e.g. a server
  * that gives all GPU memory to its KV-cache pool at start-up and allows no allocation
  * afterwards, or a loop that must not let cudaMalloc/cudaFree synchronise the device.
@@ -205,12 +222,14 @@ KIN_API kin_status kin_blocktopk_decode_static(const kin_kv_cache *cache,
                                                const kin_decode_args *args,
                                                kin_stream_t stream);
 
-/* Measurement variant of kin_blocktopk_decode (mode 0) or kin_dense_decode (mode 1):
+/* Measurement variant of kin_blocktopk_decode (mode 0), kin_dense_decode (mode 1) or
+ * kin_token_topk_decode (mode 2):
  * identical work, plus cudaEventRecord of the caller's events on `stream`: events[0]
  * before the step, events[3] after its last kernel (and, for calls that clear their
- * counters with memsets, after the clearing).  For bf16 caches the step is one kernel and events[1] and events[2] are
- * recorded right before it; for fp32 caches events[1] follows scoring and events[2]
- * selection (dense: both right after events[0]).  events: host array of 4 created
+ * counters with memsets, after the clearing).  Modes 0 and 1 on bf16 caches run one
+ * kernel, and events[1] and events[2] are recorded right before it; on fp32 caches, and in
+ * mode 2, events[1] follows scoring and events[2] selection (dense: both right after
+ * events[0]).  events: host array of 4 created
  * cudaEvent_t handles.  Used to time a step's kernels without a profiler.  While `stream`
  * is being captured into a CUDA graph the records are made with cudaEventRecordExternal,
  * so that they become event-record nodes and every replay of the graph timestamps its

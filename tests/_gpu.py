@@ -96,6 +96,22 @@ class DeviceState:
         return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy(),
                     sel=sel.cpu().numpy(), scores=scores.cpu().numpy())
 
+    def token_decode(self, budget: int, events=None):
+        """One token-level top-k decode (kin_token_topk_decode) of the current state."""
+        cfg = self.inp.cfg
+        B, Hq, H = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads
+        out = torch.full((B, Hq, cfg.head_dim), float("nan"), dtype=self.q.dtype, device=self.dev)
+        lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device=self.dev)
+        sel = torch.full((B, H, budget), -7, dtype=torch.int32, device=self.dev)
+        scores = torch.full((B, H, 16 * self.inp.max_blocks), float("nan"), dtype=torch.float32,
+                            device=self.dev)
+        K.token_topk_decode(self.cache, self.q, self.table, self.lens, budget, cfg.sm_scale,
+                            out=out, lse=lse, sel_tokens=sel, scores=scores, err_flag=self.err,
+                            events=events)
+        torch.cuda.synchronize()
+        return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy(), sel=sel.cpu().numpy(),
+                    scores=scores.cpu().numpy())
+
     def error_bits(self) -> int:
         torch.cuda.synchronize()
         return int(self.err.item())
@@ -249,3 +265,46 @@ def selection_report(inp: W.Inputs, sel: np.ndarray, c32: np.ndarray) -> dict:
                 if O.select_blocks(s16, nb, k) != kept:
                     rep["bf16_rank_diff"] += 1
     return rep
+
+
+def compare_token_rows(inp: W.Inputs, res: dict, budget: int, rows) -> dict:
+    """Compare a token-level top-k result with oracle.tokentopk row by row.
+
+    Scores: |s_gpu - s| <= SCORE_REL * sum_{g,i} |q_gi k_ti| (the kernel's group-summed fp32
+    query and 128-term fp32 dot product against the fp64 oracle).  Selection: admissible
+    (oracle.token_admissible) with tol = twice the row's largest score bound, ascending,
+    -1 padded.  Outputs: the oracle's attention over the GPU's kept set, within the bf16
+    bars."""
+    cfg = inp.cfg
+    G = cfg.group
+    stats = dict(rows=0, near_tie_rows=0, short_rows=0, max_abs=0.0)
+    for b, h in rows:
+        rp = W.row_problem(inp, b, h)
+        L = int(inp.seq_lens[b])
+        qg = rp["q"][0].astype(np.float64)
+        kk, vv = O.row_keys_values(rp["k_pages"], rp["v_pages"], rp["block_table"][0], L, 0)
+        s = O.token_scores(qg, kk)
+        bound = SCORE_REL * (np.abs(kk) @ np.abs(qg).sum(axis=0)) + 1e-30
+        sg = res["scores"][b, h, :L].astype(np.float64)
+        assert np.all(np.abs(sg - s) <= bound), f"row {(b, h)}: score error {np.abs(sg - s).max()}"
+        got = res["sel"][b, h]
+        n_keep = min(L, budget)
+        kept = [int(t) for t in got[:n_keep]]
+        assert all(int(t) == -1 for t in got[n_keep:]), f"row {(b, h)}: padding {got[n_keep:]}"
+        assert kept == sorted(kept), f"row {(b, h)}: kept positions not ascending"
+        assert O.token_admissible(s, kept, budget, 2.0 * float(bound.max())), \
+            f"row {(b, h)}: kept set not admissible"
+        if kept != O.select_tokens(s, budget):
+            stats["near_tie_rows"] += 1
+        stats["short_rows"] += L <= budget
+        o_r, l_r = O.attend(qg, kk[kept], vv[kept], cfg.sm_scale)
+        o_g = res["out"][b, h * G:(h + 1) * G].astype(np.float64)
+        err = np.abs(o_g - o_r)
+        assert np.isfinite(o_g).all(), f"row {(b, h)}: non-finite output"
+        assert err.max() <= OUT_MAX_ABS["bf16"] and err.mean() <= OUT_MEAN_ABS["bf16"], \
+            f"row {(b, h)}: output error {err.max()} / {err.mean()}"
+        lerr = np.abs(res["lse"][b, h * G:(h + 1) * G] - l_r)
+        assert lerr.max() <= LSE_ABS["bf16"], f"row {(b, h)}: lse error {lerr.max()}"
+        stats["rows"] += 1
+        stats["max_abs"] = max(stats["max_abs"], float(err.max()))
+    return stats

@@ -154,7 +154,7 @@ def test_dense_ignores_topk_and_centroids(lib):
 def test_workspace_size(lib):
     c = _cache()
     sizes = {}
-    for mode in (0, 1):
+    for mode in (0, 1, 2):
         for maxb in (1, 64, 2048):
             for k in (1, 64, 128):
                 n = ctypes.c_size_t(0)
@@ -164,11 +164,34 @@ def test_workspace_size(lib):
                 assert n.value % 256 == 0 and n.value > 0
                 sizes[mode, maxb, k] = n.value
     assert sizes[0, 2048, 128] >= sizes[0, 64, 128]
+    # token top-k: scores for every token position of every row at least
+    assert sizes[2, 2048, 128] >= 2 * 8 * 16 * 2048 * 4
     n = ctypes.c_size_t(0)
-    assert lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(_args()), 2,
+    assert lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(_args()), 3,
+                                  ctypes.byref(n)) == L.KIN_ERR_INVALID_ARG
+    assert lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(_args(top_k=0)), 2,
                                   ctypes.byref(n)) == L.KIN_ERR_INVALID_ARG
     assert lib.kin_workspace_size(ctypes.byref(c), ctypes.byref(_args()), 0,
                                   None) == L.KIN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("case,status", [
+    ("f32_cache", L.KIN_ERR_UNSUPPORTED),
+    ("append_flag", L.KIN_ERR_INVALID_ARG),
+    ("zero_budget", L.KIN_ERR_INVALID_ARG),
+    ("no_workspace", L.KIN_ERR_WORKSPACE),
+    ("no_args", L.KIN_ERR_INVALID_ARG),
+])
+def test_token_topk_validation(lib, case, status):
+    """kin_token_topk_decode's host checks, all before any device pointer is used."""
+    c = _cache(dtype=L.KIN_F32) if case == "f32_cache" else _cache()
+    a = _args(centroids=None)
+    if case == "append_flag":
+        a.flags = L.KIN_DECODE_APPEND_FINAL
+    if case == "zero_budget":
+        a.top_k = 0
+    ap = None if case == "no_args" else ctypes.byref(a)
+    assert lib.kin_token_topk_decode(ctypes.byref(c), ap, None) == status
 
 
 def test_centroid_validation(lib):
