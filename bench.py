@@ -51,6 +51,8 @@ def parse(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-shared-prefix", action="store_true",
+                    help="best-of-N loop: do not pass the prompt's blocks as the shared-prefix hint")
     ap.add_argument("--no-token", action="store_true",
                     help="skip the token-level (oracle) top-k decode of the same step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -680,10 +682,11 @@ class LoopPlan:
         self.bytes = [dw.step_bytes(lens, a) for lens, a in zip(self.lens, self.appended)]
 
 
-def run_loop(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None):
+def run_loop(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None, shared=0):
     """The best-of-N loop: step t (t >= 1) writes each sample's new token into its page
     (torch indexing: the caller's part) and advances seq_lens, then decodes; step 0 decodes
-    the initial state and restores it first, so the steps replay in a cycle."""
+    the initial state and restores it first, so the steps replay in a cycle.  shared: the
+    prompt's blocks, passed as the decode's shared-prefix hint (block top-k and dense)."""
     import torch
     import block_top_sparse_centroid_b300 as K
     dw = DeviceWorkload(cx, cfg, inp)
@@ -700,11 +703,12 @@ def run_loop(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None)
         evs[5].record()
         if dense:
             K.decode_timed(dw.cache, lp.q[t], dw.table, dw.seq, cfg.sm_scale, evs[:4], dense=True,
-                           out=dw.out, workspace=dw.wsd, err_flag=dw.err)
+                           out=dw.out, workspace=dw.wsd, err_flag=dw.err,
+                           shared_prefix_blocks=shared)
         else:
             K.decode_timed(dw.cache, lp.q[t], dw.table, dw.seq, cfg.sm_scale, evs[:4],
                            centroids=dw.cents, top_k=cfg.top_k, out=dw.out, workspace=dw.ws,
-                           err_flag=dw.err, append_final=True)
+                           err_flag=dw.err, append_final=True, shared_prefix_blocks=shared)
 
     clocks = ClockSampler(cx.dev.index)
     sp = timed_graphs(cx, [lambda e, t=t: step(t, e, False) for t in range(lp.n)], n_warm, n_steps)
@@ -719,7 +723,7 @@ def run_loop(cx, cfg, n_warm, n_steps, want_dense=True, want_e2e=True, inp=None)
     r["clocks"] = clk
     r["unique"] = unique_bytes_step0(cx, dw, lp)
     if want_e2e:
-        r["e2e"] = e2e_loop(cx, dw, lp, n_warm, n_steps)
+        r["e2e"] = e2e_loop(cx, dw, lp, n_warm, n_steps, shared)
     return r, dw
 
 
@@ -760,7 +764,7 @@ def unique_bytes_step0(cx, dw, lp) -> dict:
                     "(physical page, KV head) once although several samples read it"}
 
 
-def e2e_loop(cx, dw, lp, n_warm, n_steps) -> dict:
+def e2e_loop(cx, dw, lp, n_warm, n_steps, shared=0) -> dict:
     """The loop through the public API with host buffers: per step the token's q, k, v and
     its positions go host -> device from pinned memory, the caller writes k, v into the
     cache and advances seq_lens, one block top-k decode runs, and out comes back."""
@@ -798,7 +802,8 @@ def e2e_loop(cx, dw, lp, n_warm, n_steps) -> dict:
             dw.cache.v_pages[p_dev, :, s_dev, :] = v_dev
             dw.seq.add_(1)
         K.blocktopk_decode(dw.cache, q_dev, dw.table, dw.seq, dw.cents, cfg.top_k, cfg.sm_scale,
-                           out=dw.out, workspace=dw.ws, err_flag=dw.err, append_final=True)
+                           out=dw.out, workspace=dw.ws, err_flag=dw.err, append_final=True,
+                           shared_prefix_blocks=shared)
         out_host.copy_(dw.out, non_blocking=True)
         e1.record(stream)
         e1.synchronize()
@@ -830,9 +835,27 @@ def main() -> int:
         cpu = cpu_baseline(inp, args.cpu_seconds)
     cx = Ctx()
     loop = cfg.ctx_kind == "best_of_n" and cfg.steps > 1
-    runner = run_loop if loop else run_single
-    r, dw = runner(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e, inp)
+    shared = cfg.prefix // 16 if loop and not args.no_shared_prefix else 0
+    no_hint = None
+    if shared:
+        # the same loop without the hint, for the comparison (kernel time only), on inputs of
+        # its own (a loop advances its host inputs to its last step)
+        r0, dw0 = run_loop(cx, cfg, 5, min(args.steps, args.other_steps), False, False,
+                           W.generate(cfg), 0)
+        no_hint = {"kernel_us": r0["kernel_us"], "achieved_gbs": r0["achieved_gbs"],
+                   "frac": r0["frac"], "steps": min(args.steps, args.other_steps),
+                   "launches": r0["launches"]}
+        del dw0
+        torch.cuda.empty_cache()
+    if loop:
+        r, dw = run_loop(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e,
+                         inp, shared)
+    else:
+        r, dw = run_single(cx, cfg, args.warmup, args.steps, not args.no_dense, not args.no_e2e,
+                           inp)
     trec = traffic_record(describe(cfg))
+    if no_hint:
+        r["launches"] += no_hint["launches"]
     tok = None
     if cfg.dtype == "bf16" and not args.no_token:
         # the decode's initial state (positions below the initial lengths are untouched by
@@ -899,6 +922,12 @@ def main() -> int:
     }
     if loop:
         line["roofline"]["unique_step0"] = r["unique"]
+        line["shared_prefix"] = {
+            "blocks": shared,
+            "what": "the prompt's blocks passed as kin_decode_args.shared_prefix_blocks: their "
+                    "pages' K, V and centroid copies use the L2 evict-last policy, every other "
+                    "copy evict-first (block top-k and dense decode alike)",
+            "without_hint": no_hint}
     if others:
         line["configs"] = others
     if cpu is not None:

@@ -45,7 +45,7 @@ class DecodeArgs(ctypes.Structure):
                 ("block_table", c_void_p), ("seq_lens", c_void_p), ("centroids", c_void_p),
                 ("out", c_void_p), ("lse", c_void_p), ("sel_blocks", c_void_p),
                 ("scores", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-                ("err_flag", c_void_p), ("flags", c_int32)]
+                ("err_flag", c_void_p), ("flags", c_int32), ("shared_prefix_blocks", c_int32)]
 
 
 # Every function include/kin.h declares, with its ctypes signature.

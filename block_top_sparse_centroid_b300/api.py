@@ -197,12 +197,14 @@ class PreparedDecode:
     seq_lens updated in place), this is the low-overhead way to call the library.
 
     stream: a torch stream baked into the call, or None for the current stream of the
-    cache's device at each call."""
+    cache's device at each call.  shared_prefix_blocks: the leading logical blocks every
+    sequence shares (a Best-of-N prompt), kept in L2 for the step; a hint that changes no
+    result."""
 
     def __init__(self, mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale,
                  top_k, centroids=None, out=None, lse=None, sel_blocks=None, scores=None,
                  workspace: Optional[Workspace] = None, err_flag=None, append_final=False,
-                 stream=None):
+                 stream=None, shared_prefix_blocks: int = 0):
         lib = L.load()
         dev = cache.device
         if q.dim() != 3:
@@ -241,6 +243,7 @@ class PreparedDecode:
         a.centroids = centroids.data_ptr() if (centroids is not None and
                                                (mode == L.MODE_BLOCKTOPK or append_final)) else None
         a.flags = L.KIN_DECODE_APPEND_FINAL if append_final else 0
+        a.shared_prefix_blocks = int(shared_prefix_blocks)
         a.out = out.data_ptr()
         a.lse = None if lse is None else lse.data_ptr()
         a.sel_blocks = None if (sel_blocks is None or mode == L.MODE_DENSE) else sel_blocks.data_ptr()
@@ -278,9 +281,10 @@ class PreparedDecode:
 
 def _decode(mode: int, cache: PagedKVCache, q, block_table, seq_lens, sm_scale, top_k,
             centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream, events=None,
-            append_final=False):
+            append_final=False, shared_prefix_blocks=0):
     call = PreparedDecode(mode, cache, q, block_table, seq_lens, sm_scale, top_k, centroids,
-                          out, lse, sel_blocks, scores, workspace, err_flag, append_final)
+                          out, lse, sel_blocks, scores, workspace, err_flag, append_final,
+                          shared_prefix_blocks=shared_prefix_blocks)
     if events is not None:
         return call.timed(list(events), stream)
     return call(stream)
@@ -294,21 +298,24 @@ def prepare_blocktopk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: 
                              scores: Optional[torch.Tensor] = None,
                              workspace: Optional[Workspace] = None,
                              err_flag: Optional[torch.Tensor] = None,
-                             append_final: bool = False, stream=None) -> PreparedDecode:
+                             append_final: bool = False, stream=None,
+                             shared_prefix_blocks: int = 0) -> PreparedDecode:
     """A block top-k decode call (kin_blocktopk_decode) prepared once, run by calling it."""
     return PreparedDecode(L.MODE_BLOCKTOPK, cache, q, block_table, seq_lens, sm_scale, top_k,
                           centroids, out, lse, sel_blocks, scores, workspace, err_flag,
-                          append_final, stream)
+                          append_final, stream, shared_prefix_blocks)
 
 
 def prepare_dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
                          seq_lens: torch.Tensor, sm_scale: float,
                          out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                          workspace: Optional[Workspace] = None,
-                         err_flag: Optional[torch.Tensor] = None, stream=None) -> PreparedDecode:
+                         err_flag: Optional[torch.Tensor] = None, stream=None,
+                         shared_prefix_blocks: int = 0) -> PreparedDecode:
     """A dense decode call (kin_dense_decode) prepared once, run by calling it."""
     return PreparedDecode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, None,
-                          out, lse, None, None, workspace, err_flag, False, stream)
+                          out, lse, None, None, workspace, err_flag, False, stream,
+                          shared_prefix_blocks)
 
 
 def prepare_token_topk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
@@ -361,14 +368,16 @@ def blocktopk_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Te
                      scores: Optional[torch.Tensor] = None,
                      workspace: Optional[Workspace] = None,
                      err_flag: Optional[torch.Tensor] = None, stream=None,
-                     append_final: bool = False) -> torch.Tensor:
+                     append_final: bool = False, shared_prefix_blocks: int = 0) -> torch.Tensor:
     """One block top-k decode step (score, select, sparse attention): kin_blocktopk_decode.
 
     append_final: also write the centroid of each sequence's final block when that block
-    is complete (KIN_DECODE_APPEND_FINAL), i.e. the append the next steps need."""
+    is complete (KIN_DECODE_APPEND_FINAL), i.e. the append the next steps need.
+    shared_prefix_blocks: the leading logical blocks all sequences share (their pages are
+    kept in L2 for the step; results do not depend on it)."""
     return _decode(L.MODE_BLOCKTOPK, cache, q, block_table, seq_lens, sm_scale, top_k,
                    centroids, out, lse, sel_blocks, scores, workspace, err_flag, stream,
-                   append_final=append_final)
+                   append_final=append_final, shared_prefix_blocks=shared_prefix_blocks)
 
 
 def decode_timed(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
@@ -376,13 +385,13 @@ def decode_timed(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor
                  centroids: Optional[torch.Tensor] = None, top_k: int = 1,
                  out: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
                  err_flag: Optional[torch.Tensor] = None, stream=None,
-                 append_final: bool = False) -> torch.Tensor:
+                 append_final: bool = False, shared_prefix_blocks: int = 0) -> torch.Tensor:
     """One decode step that also records 4 torch.cuda.Events around its kernels
     (before scoring, after scoring, after selection, after attention): kin_decode_timed."""
     mode = L.MODE_DENSE if dense else L.MODE_BLOCKTOPK
     return _decode(mode, cache, q, block_table, seq_lens, sm_scale, top_k, centroids, out,
                    None, None, None, workspace, err_flag, stream, events=list(events),
-                   append_final=append_final)
+                   append_final=append_final, shared_prefix_blocks=shared_prefix_blocks)
 
 
 def dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor,
@@ -390,8 +399,8 @@ def dense_decode(cache: PagedKVCache, q: torch.Tensor, block_table: torch.Tensor
                  lse: Optional[torch.Tensor] = None, workspace: Optional[Workspace] = None,
                  err_flag: Optional[torch.Tensor] = None, stream=None,
                  centroids: Optional[torch.Tensor] = None,
-                 append_final: bool = False) -> torch.Tensor:
+                 append_final: bool = False, shared_prefix_blocks: int = 0) -> torch.Tensor:
     """Dense paged decode over every block (the comparison baseline): kin_dense_decode."""
     return _decode(L.MODE_DENSE, cache, q, block_table, seq_lens, sm_scale, 1, centroids,
                    out, lse, None, None, workspace, err_flag, stream,
-                   append_final=append_final)
+                   append_final=append_final, shared_prefix_blocks=shared_prefix_blocks)

@@ -1155,7 +1155,11 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
   using C = Cfg<D, NT>;
   const int lane = threadIdx.x & 31, q = (threadIdx.x >> 5) - C::kCW;
   const bool leader = q == 0;
+  // Every copy streams (evict-first), except the pages of the leading blocks that all
+  // sequences share (a Best-of-N prompt), which stay in L2 for the step's other readers.
   const uint64_t policy = l2_policy_evict_first();
+  const uint64_t keep_policy = l2_policy_evict_last();
+  const int shared_j = p.shared_prefix_blocks;
   const int H = p.num_kv_heads;
   const int total = p.n_score_items + p.n_select_items + p.n_attn_items;
   uint32_t pos[C::kPPC] = {};  // sub-ring position of each of the pipeline's consumers
@@ -1290,7 +1294,7 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
         if (pg >= 0)
           bulk_load(ring + s * R::kStageBytes + lane * row_bytes,
                     p.centroids + (static_cast<int64_t>(pg) * H + h0) * D, row_bytes, &sh.full[s],
-                    policy);
+                    j0 + pa + lane < shared_j ? keep_policy : policy);
         KIN_TOC(kTrPIssue, t_issue);
       }
     } else if (d.kind == kDescAttn) {
@@ -1329,9 +1333,10 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
           }
         }
         const int i = base + lane * kProducers;
-        int page = -1, ntok = 0;
+        int page = -1, ntok = 0, jblk = -1;
         if (i < cnt) {
           const int j = every_block ? i0 + i : __ldcg(srow + i0 + i);
+          jblk = j;
           if (j >= 0 && j < nb) {
             const int pg = __ldg(trow + j);
             if (pg >= 0 && pg < p.num_pages) {
@@ -1363,6 +1368,8 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
           if (lane == l + kPrefetchPages) prefetch_page();
           const int pg = __shfl_sync(0xffffffffu, page, l);
           const int nt = __shfl_sync(0xffffffffu, ntok, l);
+          const int jb = __shfl_sync(0xffffffffu, jblk, l);
+          const bool shared = jb >= 0 && jb < shared_j;
           int s = 0;
           const int cc = ((base - q) / kProducers + l) % C::kPPC;
           if (lane == 0) s = claim(cc, make_int4(pg, nt, 0, 0), pg >= 0 ? R::kStageBytes : 0u);
@@ -1371,10 +1378,11 @@ __device__ void producer(const FusedParams &p, const CUtensorMap *kmap, const CU
           if (pg >= 0 && lane < 2) {   // lane 0: K, lane 1: V; one copy per page each
             uint8_t *dst = ring + s * R::kStageBytes + (lane ? BfTile<D>::kKBytes : 0);
             const CUtensorMap *map = lane ? vmap : kmap;
+            const uint64_t pol = shared ? keep_policy : policy;
             if (D == 128)
-              tma_load_3d(dst, map, 0, pg * H * kBlock + ybase, 0, &sh.full[s], policy);
+              tma_load_3d(dst, map, 0, pg * H * kBlock + ybase, 0, &sh.full[s], pol);
             else
-              tma_load_2d(dst, map, 0, pg * H * kBlock + ybase, &sh.full[s], policy);
+              tma_load_2d(dst, map, 0, pg * H * kBlock + ybase, &sh.full[s], pol);
           }
           KIN_TOC(kTrPIssue, t_issue);
           KIN_COUNT(kTrPPages, 1);

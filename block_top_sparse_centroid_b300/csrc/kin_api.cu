@@ -194,6 +194,9 @@ kin_status check_args(const kin_kv_cache *c, const kin_decode_args *a, int mode)
   if (!aligned16(a->q)) return fail(KIN_ERR_INVALID_ARG, "q must be 16-byte aligned");
   if ((a->flags & ~KIN_DECODE_APPEND_FINAL) != 0)
     return fail(KIN_ERR_INVALID_ARG, "unknown flags 0x%x", static_cast<unsigned>(a->flags));
+  if (a->shared_prefix_blocks < 0 || a->shared_prefix_blocks > a->max_blocks)
+    return fail(KIN_ERR_INVALID_ARG, "shared_prefix_blocks %d outside 0..max_blocks (%d)",
+                a->shared_prefix_blocks, a->max_blocks);
   if (mode == 0 || (a->flags & KIN_DECODE_APPEND_FINAL) != 0) {
     if (a->centroids == nullptr) return fail(KIN_ERR_INVALID_ARG, "centroids must not be NULL");
     if (!aligned16(a->centroids)) return fail(KIN_ERR_INVALID_ARG, "centroids must be 16-byte aligned");
@@ -529,6 +532,7 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     }
 
     fp.append_final = append;
+    fp.shared_prefix_blocks = a->shared_prefix_blocks;
     fp.sm_scale = a->sm_scale;
     // One launch: score, select and attention items through one work queue, so the
     // scoring of later rows overlaps the attention of earlier ones.

@@ -100,6 +100,7 @@ struct FusedParams {
   int lag_select, lag_attn;
   int coop_select;                 // select items are single rows, selected by all consumer warps
   int append_final;
+  int shared_prefix_blocks;        // leading logical blocks read with the evict-last policy
   float sm_scale;
 };
 // Token-level top-k decode (bf16 caches): score every token, select the top_k per row,

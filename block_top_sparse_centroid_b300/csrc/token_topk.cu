@@ -149,6 +149,7 @@ __global__ void __launch_bounds__(kTsThreads) token_score_kernel(TokenParams p) 
 // longer than 1024 x 32 positions go through token_select_long.
 template <int KPT, int NTHR>
 __global__ void __launch_bounds__(NTHR) token_select_kernel(TokenParams p) {
+  static_assert(KPT % kBlock == 0 || kBlock % KPT == 0, "a thread's run stays within whole pages");
   __shared__ int hist[256];
   __shared__ int scan_tmp[32];
   __shared__ uint32_t s_prefix;
@@ -186,6 +187,15 @@ __global__ void __launch_bounds__(NTHR) token_select_kernel(TokenParams p) {
   }
   const float *srow = p.scores + static_cast<int64_t>(row) * p.score_stride;
   const int t0 = tid * KPT;
+  // the pages of this thread's run (KPT is a multiple of 16 or divides it, so the run
+  // covers at most kRunPages pages), read now so that the emission waits on no load
+  constexpr int kRunPages = KPT >= kBlock ? KPT / kBlock : 1;
+  int run_pg[kRunPages];
+#pragma unroll
+  for (int u = 0; u < kRunPages; ++u) {
+    const int t = t0 + u * kBlock;
+    run_pg[u] = t < L ? trow[t / kBlock] : -1;
+  }
   uint32_t key[KPT];   // 0: no position (past L)
 #pragma unroll
   for (int i = 0; i < KPT; i += 4) {
@@ -259,7 +269,14 @@ __global__ void __launch_bounds__(NTHR) token_select_kernel(TokenParams p) {
       keep = true;
       ++used_eq;
     }
-    if (keep) emit(w++, t0 + i);
+    if (keep) {
+      const int t = t0 + i;
+      const int pg = run_pg[i / kBlock < kRunPages ? i / kBlock : kRunPages - 1];
+      const bool ok = pg >= 0 && pg < p.num_pages;
+      gat[w] = ok ? (pg * H + h) * kBlock + t % kBlock : -1;
+      if (usr != nullptr) usr[w] = t;
+      ++w;
+    }
   }
 }
 

@@ -121,6 +121,14 @@ typedef struct {
   size_t workspace_bytes;
   int32_t *err_flag;      /* optional device int; KIN_DEVERR_* bits are OR-ed in       */
   int32_t flags;          /* KIN_DECODE_* bits, 0 for none                             */
+  int32_t shared_prefix_blocks; /* 0..max_blocks: the leading logical blocks whose pages
+                             every sequence of the batch shares (a Best-of-N prompt).
+                             Block top-k and dense decode then keep those pages' K, V and
+                             centroid rows in L2 for the whole step (evict-last copies,
+                             every other copy streams evict-first), so that HBM serves
+                             each shared page once per step however many sequences read
+                             it.  A hint: results are identical for any value; 0 = none.
+                             Ignored by kin_token_topk_decode                           */
 } kin_decode_args;
 
 /* Decode flag: when a sequence's final block is complete (seq_len a multiple of 16: the

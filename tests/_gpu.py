@@ -75,7 +75,7 @@ class DeviceState:
     def refresh_q(self):
         self.q = self.inp.q.to(self.dev)
 
-    def decode(self, dense=False, append_final=False):
+    def decode(self, dense=False, append_final=False, shared_prefix_blocks=0):
         cfg = self.inp.cfg
         B, Hq, H = cfg.batch, cfg.num_q_heads, cfg.num_kv_heads
         out = torch.full((B, Hq, cfg.head_dim), float("nan"), dtype=self.q.dtype, device=self.dev)
@@ -83,7 +83,7 @@ class DeviceState:
         if dense:
             K.dense_decode(self.cache, self.q, self.table, self.lens, cfg.sm_scale, out=out,
                            lse=lse, err_flag=self.err, centroids=self.cents,
-                           append_final=append_final)
+                           append_final=append_final, shared_prefix_blocks=shared_prefix_blocks)
             torch.cuda.synchronize()
             return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy())
         sel = torch.full((B, H, cfg.top_k), -7, dtype=torch.int32, device=self.dev)
@@ -91,7 +91,8 @@ class DeviceState:
                             device=self.dev)
         K.blocktopk_decode(self.cache, self.q, self.table, self.lens, self.cents, cfg.top_k,
                            cfg.sm_scale, out=out, lse=lse, sel_blocks=sel, scores=scores,
-                           err_flag=self.err, append_final=append_final)
+                           err_flag=self.err, append_final=append_final,
+                           shared_prefix_blocks=shared_prefix_blocks)
         torch.cuda.synchronize()
         return dict(out=out.float().cpu().numpy(), lse=lse.cpu().numpy(),
                     sel=sel.cpu().numpy(), scores=scores.cpu().numpy())

@@ -133,6 +133,8 @@ def test_status_names(lib):
     (dict(args_kw=dict(centroids=None)), L.KIN_ERR_INVALID_ARG),
     (dict(args_kw=dict(seq_lens=None)), L.KIN_ERR_INVALID_ARG),
     (dict(args_kw=dict(flags=2)), L.KIN_ERR_INVALID_ARG),
+    (dict(args_kw=dict(shared_prefix_blocks=-1)), L.KIN_ERR_INVALID_ARG),
+    (dict(args_kw=dict(shared_prefix_blocks=65)), L.KIN_ERR_INVALID_ARG),
     (dict(), L.KIN_ERR_WORKSPACE),                                   # no workspace
     (dict(args_kw=dict(workspace=0x10000, workspace_bytes=16)), L.KIN_ERR_WORKSPACE),
     (dict(args_kw=dict(workspace=0x10010, workspace_bytes=1 << 30)), L.KIN_ERR_WORKSPACE),
