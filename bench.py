@@ -53,6 +53,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-shared-prefix", action="store_true",
                     help="best-of-N loop: do not pass the prompt's blocks as the shared-prefix hint")
+    ap.add_argument("--no-hint-compare", action="store_true",
+                    help="best-of-N loop: skip the comparison run without the shared-prefix hint")
     ap.add_argument("--no-token", action="store_true",
                     help="skip the token-level (oracle) top-k decode of the same step")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -837,7 +839,7 @@ def main() -> int:
     loop = cfg.ctx_kind == "best_of_n" and cfg.steps > 1
     shared = cfg.prefix // 16 if loop and not args.no_shared_prefix else 0
     no_hint = None
-    if shared:
+    if shared and not args.no_hint_compare:
         # the same loop without the hint, for the comparison (kernel time only), on inputs of
         # its own (a loop advances its host inputs to its last step)
         r0, dw0 = run_loop(cx, cfg, 5, min(args.steps, args.other_steps), False, False,

@@ -500,13 +500,14 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
     fp.items_per_split = pl.items_per_split;
     fp.splits_per_row = pl.max_splits;
     fp.n_score_items = mode == 0 ? a->batch * pl.head_ranges * pl.chunks_per_seq : 0;
-    // With no more rows than CTAs, a row's selection is on the critical path (there is too
+    // With up to two rows per CTA, a row's selection is on the critical path (there is too
     // little other attention work to hide it), so all consumer warps of a CTA select one
     // row, one row per select item: ~4-5 us for 2047 candidates instead of ~17 us for a
     // warp alone.  With more rows the cheaper one-warp-per-row selection of a whole head
-    // range per item wins (measured: 32K-token rows, 128 rows 9 % faster cooperative,
-    // 256 rows 5 % slower).
-    fp.coop_select = pl.rows <= kPlanSMs ? 1 : 0;
+    // range per item wins.  Measured with the in-selection re-scoring: 256 rows of 32K
+    // tokens 9 % faster cooperative than one warp per row; 2048 rows of 3K-17K tokens 21 %
+    // slower.
+    fp.coop_select = pl.rows <= 2 * kPlanSMs ? 1 : 0;
     fp.n_select_items = mode == 0 ? a->batch * (fp.coop_select ? c->num_kv_heads : pl.head_ranges) : 0;
     fp.n_attn_items = pl.rows * pl.max_splits;
     // Queue lags in rounds (one sequence per round).  At the start every CTA takes an item
@@ -519,7 +520,7 @@ kin_status run_decode(const kin_kv_cache *c, const kin_decode_args *a, int mode,
       const int span = 2 * kPlanSMs;
       fp.lag_select = s_per > 0 ? (span + s_per - 1) / s_per : 0;
       fp.lag_attn = fp.lag_select + (span + s_per + sel_per - 1) / (s_per + sel_per);
-      if (fp.coop_select) {
+      if (pl.rows <= kPlanSMs) {
         // No more rows than CTAs: every row's selection runs on a CTA of its own anyway, so
         // the queue takes all score items, then all select items, then all attention items
         // (measured: 16 sequences of 8K-32K tokens 12 % faster than interleaved, 8

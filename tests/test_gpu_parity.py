@@ -49,22 +49,25 @@ def test_group_and_head_dim(d, G):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("G", [1, 5])
-def test_eight_head_ranges(d, G):
-    # 8 KV heads: the score stages of a whole 8-head range (four lanes per centroid); with
-    # 19 sequences (152 rows, more than the 148 CTAs) one warp selects each row of a range
+@pytest.mark.parametrize("copies", [1, 2])
+def test_eight_head_ranges(d, G, copies):
+    # 8 KV heads: the score stages of a whole 8-head range (four lanes per centroid); 19
+    # sequences (152 rows, at most two per CTA): cooperative selection of each row; 38
+    # sequences (304 rows, more than two per CTA): one warp selects each row of a range
     lens = (130, 1500, 4097, 2048, 17, 700, 16 * 33, 999, 3000, 64,
-            1201, 250, 16 * 90 + 1, 3333, 160, 2222, 801, 47, 1024)
-    cfg = _cfg(f"h8g{G}d{d}", d=d, H=8, G=G, k=8, lens=lens, seed=G * 10 + d)
+            1201, 250, 16 * 90 + 1, 3333, 160, 2222, 801, 47, 1024) * copies
+    cfg = _cfg(f"h8g{G}d{d}x{copies}", d=d, H=8, G=G, k=8, lens=lens, seed=G * 10 + d)
     _run(cfg)
 
 
-@pytest.mark.parametrize("H", [4, 16])
-def test_other_head_range_widths(H):
+@pytest.mark.parametrize("H,copies", [(4, 1), (16, 1), (16, 2)])
+def test_other_head_range_widths(H, copies):
     # 4 heads (40 rows): the queries of the range in registers, cooperative selection;
-    # 16 heads (160 rows, more than the 148 CTAs): queries read from global memory into one
-    # shared copy, two pages per score stage, two rows per selecting warp
-    lens = (130, 1500, 4097, 700, 2048, 33, 1111, 16 * 50, 2500, 401)
-    cfg = _cfg(f"h{H}", H=H, G=2, k=8, lens=lens, seed=H)
+    # 16 heads: queries read from global memory into one shared copy, two pages per score
+    # stage; 160 rows: cooperative selection; 320 rows (more than two per CTA): two rows
+    # per selecting warp
+    lens = (130, 1500, 4097, 700, 2048, 33, 1111, 16 * 50, 2500, 401) * copies
+    cfg = _cfg(f"h{H}x{copies}", H=H, G=2, k=8, lens=lens, seed=H)
     _run(cfg)
     _run(cfg, dense=True)
 

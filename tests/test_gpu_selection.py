@@ -2,14 +2,14 @@
 
 * Long rows: more candidates than the selecting warp (2048) or CTA (4096 with 8 consumer
   warps, 2048 with 4) holds in registers, up to the largest row the library accepts
-  (16383 candidates), with one warp per row (more rows than CTAs) and with cooperative
-  selection (fewer rows than CTAs).  Checked against the oracle's fp32-centroid
+  (16383 candidates), with one warp per row (more than two rows per CTA) and with
+  cooperative selection (at most two).  Checked against the oracle's fp32-centroid
   selection and attention.
 * Rows where only the second centroid code can rank the candidates: every block's mean
   rounds to the same bf16 value, and the fp32 means differ by more than the near-tie band.
   A selection from the first code alone would keep the lowest indices; the library must
-  keep the oracle's blocks exactly, on every path (ambiguous candidates re-scored from a
-  list, and more of them than a list holds).
+  keep the oracle's blocks exactly, on every path (ambiguous candidates re-scored from the
+  selection's shared-memory list of 256, and more of them than the list holds).
 """
 import math
 
@@ -42,8 +42,9 @@ def _check_all(inp, res, sample=None):
 @pytest.mark.parametrize("case", ["warp_rows", "cta8_rows", "cta4_rows", "max_blocks"])
 def test_long_rows(case):
     if case == "warp_rows":
-        # 152 rows (> 148 CTAs): one warp per row, 2062..2499 candidates (> 2048 in registers)
-        lens = tuple(33000 + 373 * i for i in range(19))
+        # 304 rows (> 2 x 148 CTAs): one warp per row, 2062..2499 candidates (> 2048 in
+        # registers)
+        lens = tuple(33000 + 187 * i for i in range(38))
         cfg = _cfg("long-warp", lens, H=8, G=1, d=64, k=24, seed=31)
         sample = 10
     elif case == "cta8_rows":
@@ -93,13 +94,13 @@ def _residual_decides(inp, high_frac_rows, k, seed):
 
 @pytest.mark.parametrize("case", ["warp_list", "warp_over_cap", "cta_list", "cta_over_cap"])
 def test_second_code_decides_selection(case):
-    if case == "warp_list":          # 152 rows, one warp each, 100 ambiguous candidates
-        cfg = _cfg("res-warp", (16 * 101,) * 19, H=8, G=2, d=64, k=40, seed=41)
-    elif case == "warp_over_cap":    # 152 rows, 600 ambiguous candidates (> 256 listed)
-        cfg = _cfg("res-warp-big", (16 * 601,) * 19, H=8, G=1, d=64, k=40, seed=42)
-    elif case == "cta_list":         # 4 rows, cooperative, 700 ambiguous (<= 1024 listed)
-        cfg = _cfg("res-cta", (16 * 701, 16 * 500 + 3), H=2, G=4, k=64, seed=43)
-    else:                            # 2 rows, cooperative, 2000 ambiguous (> 1024 listed)
+    if case == "warp_list":          # 304 rows, one warp each, 100 ambiguous candidates
+        cfg = _cfg("res-warp", (16 * 101,) * 38, H=8, G=2, d=64, k=40, seed=41)
+    elif case == "warp_over_cap":    # 304 rows, 600 ambiguous candidates (> 256 listed)
+        cfg = _cfg("res-warp-big", (16 * 601,) * 38, H=8, G=1, d=64, k=40, seed=42)
+    elif case == "cta_list":         # 4 rows, cooperative, 150-200 ambiguous (<= 256 listed)
+        cfg = _cfg("res-cta", (16 * 201, 16 * 150 + 3), H=2, G=4, k=64, seed=43)
+    else:                            # 2 rows, cooperative, 2000 ambiguous (> 256 listed)
         cfg = _cfg("res-cta-big", (16 * 2001, 16 * 1500 + 9), H=1, G=8, k=100, seed=44)
     inp = W.generate(cfg)
     _residual_decides(inp, 0.5, cfg.top_k, seed=cfg.seed)
