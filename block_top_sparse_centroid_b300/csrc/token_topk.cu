@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kTsThreads) token_score_kernel(TokenParams p) 
 // keys in registers, loaded once with 16-byte reads: four radix passes of 8 bits find the
 // B-th largest key (counts per digit aggregated per warp before the shared-memory
 // atomics), then two block scans place every kept position in ascending order.  Rows
-// longer than 1024 x 32 positions go through token_select_long.
+// longer than 1024 x 32 positions go through token_select_long; rows of 8K-25.6K positions
+// go through token_select_smem, which fits more of them on an SM.
 template <int KPT, int NTHR>
 __global__ void __launch_bounds__(NTHR) token_select_kernel(TokenParams p) {
   static_assert(KPT % kBlock == 0 || kBlock % KPT == 0, "a thread's run stays within whole pages");
@@ -277,6 +278,127 @@ __global__ void __launch_bounds__(NTHR) token_select_kernel(TokenParams p) {
       if (usr != nullptr) usr[w] = t;
       ++w;
     }
+  }
+}
+
+// The same selection with the row's keys and page ids in shared memory instead of
+// registers (512 threads, few registers): for rows whose keys take at most ~100 KB, two or
+// more rows then run on one SM (the register-resident version above fits one 1024-thread
+// CTA per SM once a row exceeds 512 x 32 positions).  Radix passes walk the keys in a
+// strided order (conflict-free); the compaction walks contiguous runs.
+constexpr int kSelSmemThreads = 512;
+constexpr int kSelSmemMaxKeys = 25600;   // 100 KB of keys
+
+__global__ void __launch_bounds__(kSelSmemThreads) token_select_smem(TokenParams p) {
+  extern __shared__ uint32_t skeys[];   // [16 max_blocks] keys, then [max_blocks] pages
+  __shared__ int hist[256];
+  __shared__ int scan_tmp[32];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_remaining;
+  const int row = blockIdx.x;
+  const int H = p.num_kv_heads;
+  const int b = row / H, h = row % H;
+  const int B = p.top_k;
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+  int32_t *gat = p.gather + static_cast<int64_t>(row) * B;
+  int32_t *usr = p.sel_out == nullptr ? nullptr : p.sel_out + static_cast<int64_t>(row) * B;
+  const int L = p.seq_lens[b];
+  const int32_t *trow = p.block_table + static_cast<int64_t>(b) * p.max_blocks;
+  auto pad = [&](int from) {
+    for (int i = from + tid; i < B; i += nt) {
+      gat[i] = -1;
+      if (usr != nullptr) usr[i] = -1;
+    }
+  };
+  if (L < 1 || L > kBlock * p.max_blocks) {
+    pad(0);
+    return;
+  }
+  const int nb = (L + kBlock - 1) / kBlock;
+  int *spages = reinterpret_cast<int *>(skeys + kBlock * p.max_blocks);
+  for (int j = tid; j < nb; j += nt) spages[j] = trow[j];
+  auto emit = [&](int pos, int t) {
+    const int pg = spages[t / kBlock];
+    const bool ok = pg >= 0 && pg < p.num_pages;
+    gat[pos] = ok ? (pg * H + h) * kBlock + t % kBlock : -1;
+    if (usr != nullptr) usr[pos] = t;
+  };
+  if (L <= B) {
+    __syncthreads();
+    for (int i = tid; i < L; i += nt) emit(i, i);
+    pad(L);
+    return;
+  }
+  const float *srow = p.scores + static_cast<int64_t>(row) * p.score_stride;
+  for (int i = 4 * tid; i < L; i += 4 * nt) {   // rows start 16-byte aligned
+    if (i + 3 < L) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(srow + i));
+      skeys[i] = token_key(v.x);
+      skeys[i + 1] = token_key(v.y);
+      skeys[i + 2] = token_key(v.z);
+      skeys[i + 3] = token_key(v.w);
+    } else {
+      for (int u = 0; u < 4 && i + u < L; ++u) skeys[i + u] = token_key(__ldcg(srow + i + u));
+    }
+  }
+  if (tid == 0) {
+    s_prefix = 0u;
+    s_remaining = B;
+  }
+  uint32_t mask = 0u;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += nt) hist[i] = 0;
+    __syncthreads();   // (first pass: also the keys and pages in shared memory)
+    const uint32_t prefix = s_prefix;
+#pragma unroll 4
+    for (int t0 = 0; t0 < L; t0 += nt) {
+      const int t = t0 + tid;
+      const uint32_t key = t < L ? skeys[t] : 0u;
+      const bool in = t < L && (key & mask) == prefix;
+      const unsigned active = __ballot_sync(0xffffffffu, in);
+      if (in) {
+        const uint32_t dig = (key >> shift) & 255u;
+        const unsigned same = __match_any_sync(active, dig);
+        if (lane == __ffs(same) - 1) atomicAdd(&hist[dig], __popc(same));
+      }
+    }
+    __syncthreads();
+    const int cnt = tid < 256 ? hist[255 - tid] : 0;
+    int total;
+    const int above = block_exclusive_scan(cnt, scan_tmp, &total);
+    const int remaining = s_remaining;
+    __syncthreads();
+    if (tid < 256 && above < remaining && above + cnt >= remaining) {
+      s_prefix = prefix | (static_cast<uint32_t>(255 - tid) << shift);
+      s_remaining = remaining - above;
+    }
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  const uint32_t thr = s_prefix;
+  const int take_eq = s_remaining;
+  const int per = (L + nt - 1) / nt;
+  const int lo = min(L, tid * per), hi = min(L, lo + per);
+  int gt = 0, eq = 0;
+  for (int t = lo; t < hi; ++t) {
+    const uint32_t key = skeys[t];
+    gt += key > thr ? 1 : 0;
+    eq += key == thr ? 1 : 0;
+  }
+  int tot;
+  const int eq_before = block_exclusive_scan(eq, scan_tmp, &tot);
+  const int my_eq = max(0, min(eq, take_eq - eq_before));
+  int w = block_exclusive_scan(gt + my_eq, scan_tmp, &tot);
+  int used_eq = 0;
+  for (int t = lo; t < hi; ++t) {
+    const uint32_t key = skeys[t];
+    bool keep = key > thr;
+    if (key == thr && used_eq < my_eq) {
+      keep = true;
+      ++used_eq;
+    }
+    if (keep) emit(w++, t);
   }
 }
 
@@ -528,12 +650,26 @@ cudaError_t launch_token_select(const TokenParams &p, cudaStream_t stream) {
   // keys per thread: the smallest register run that covers the longest possible row
   const int64_t longest = static_cast<int64_t>(kBlock) * p.max_blocks;
   const int rows = p.batch * p.num_kv_heads;
+  if (longest > 512 * 16 && longest <= kSelSmemMaxKeys) {
+    // keys in shared memory: two to three rows per SM instead of one 1024-thread CTA
+    const size_t smem = sizeof(uint32_t) * static_cast<size_t>(longest + p.max_blocks);
+    static int set_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (set_device != dev) {
+      e = cudaFuncSetAttribute(token_select_smem, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(sizeof(uint32_t) * (kSelSmemMaxKeys + kSelSmemMaxKeys / kBlock)));
+      if (e != cudaSuccess) return e;
+      set_device = dev;
+    }
+    token_select_smem<<<rows, kSelSmemThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   if (longest <= 512 * 8)
     token_select_kernel<8, 512><<<rows, 512, 0, stream>>>(p);
   else if (longest <= 512 * 16)
     token_select_kernel<16, 512><<<rows, 512, 0, stream>>>(p);
-  else if (longest <= 512 * 32)
-    token_select_kernel<32, 512><<<rows, 512, 0, stream>>>(p);
   else if (longest <= 1024 * 32)
     token_select_kernel<32, 1024><<<rows, 1024, 0, stream>>>(p);
   else

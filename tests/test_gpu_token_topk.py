@@ -59,7 +59,8 @@ def _all(cfg):
     (128, 1, 4, (4000, 90), 1),                        # one kept token, one query head
     (64, 8, 2, (5000, 4999), 1024),                    # several attention splits per row
     (128, 5, 2, (600, 37), 1024),                      # every row shorter than the budget
-    (128, 2, 2, (12000, 900), 2000),                   # 32 keys per thread, 512 threads
+    (128, 2, 2, (12000, 900), 2000),                   # keys in shared memory (8K-25.6K)
+    (64, 2, 1, (30000, 2000), 800),                    # 32 keys per thread, 1024 threads
     (64, 2, 1, (40000, 3000), 500),                    # longer than the register-resident select
 ])
 def test_token_topk_parity(d, G, H, lens, budget):
