@@ -1507,7 +1507,7 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
     }
   }
   const float score = butterfly(v);
-  // lane c: sum_i |qs_i| 2^e(c1_i) of centroid c (row_bound) from its own row, 16-byte
+  // lane c: sum_i |qs_i| |c1_i| of centroid c (row_bound) from its own row, 16-byte
   // chunks in an order rotated by the lane (rows are 2 D bytes apart, so 8 consecutive
   // lanes read 8 distinct bank groups)
   float acc_b = 0.f;
@@ -1518,7 +1518,7 @@ __device__ __forceinline__ float stage_scores(const uint8_t *stage, const QRegs<
       float f[8];
       Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(own + cr * 16), f);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) acc_b += fabsf(qown[8 * cr + k] * pow2_floor(f[k]));
+      for (int k = 0; k < 8; ++k) acc_b = fmaf(fabsf(qown[8 * cr + k]), fabsf(f[k]), acc_b);
     }
   }
   hb = acc_b;
@@ -1578,8 +1578,8 @@ __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSli
       for (int k = 0; k < 8; k += 2) {
         a0 = fmaf(qv.v[c * 8 + k], f[k], a0);
         a1 = fmaf(qv.v[c * 8 + k + 1], f[k + 1], a1);
-        n0 += fabsf(qv.v[c * 8 + k] * pow2_floor(f[k]));
-        n1 += fabsf(qv.v[c * 8 + k + 1] * pow2_floor(f[k + 1]));
+        n0 = fmaf(fabsf(qv.v[c * 8 + k]), fabsf(f[k]), n0);
+        n1 = fmaf(fabsf(qv.v[c * 8 + k + 1]), fabsf(f[k + 1]), n1);
       }
     }
     acc[pp] = a0 + a1;
@@ -1607,13 +1607,13 @@ __device__ __forceinline__ void stage_scores_h8(const uint8_t *stage, const QSli
 // kernel computes from the first centroid code c1 (bf16) and s* the exact score of the
 // fp32 mean c.  c1_i is c_i rounded to nearest with 8 significant bits, so for a normal
 // c1_i in [2^e, 2^(e+1)] the error |c_i - c1_i| is at most half a unit in the last place
-// of c_i's binade, <= 2^(e-8) = 2^-8 pow2_floor(c1_i); hence
-// |s - s*| <= 2^-8 hb with hb = sum_i |qs_i| pow2_floor(c1_i), which the score stage sums
-// per centroid (exact products of powers of two).  fp32 rounding of the score's products
-// and sums, of hb and of qs itself stays below 2^-15 hb for d <= 128 and G <= 16
-// (|c1_i| < 2 pow2_floor(c1_i)).  kBoundScale = 2^-8 + 2^-12 covers both.  A zero or
-// subnormal c1_i (pow2_floor 0) is off by at most 2^-134, which the 1e-30 |qs|_1 term
-// covers.
+// of c_i's binade, <= 2^(e-8) <= 2^-8 |c1_i|; hence |s - s*| <= 2^-8 hb with
+// hb = sum_i |qs_i| |c1_i|, which the score stage sums per centroid (one multiply-add per
+// element, the absolute values being operand modifiers).  fp32 rounding of the score's
+// products and sums, of hb and of qs itself stays below 2^-15 hb for d <= 128 and G <= 16.
+// kBoundScale = 2^-8 + 2^-12 covers both.  A zero or subnormal c1_i is off by at most
+// 2^-134, which the 1e-30 |qs|_1 term covers.  (Summing 2^e instead of |c1_i| gives a
+// bound up to half as large, but costs a mask per element: measured slower.)
 constexpr float kBoundScale = 0.00415039062f;   // 2^-8 + 2^-12, exact in fp32
 __device__ __forceinline__ float row_bound(float qn1, float hb) {
   return kBoundScale * hb + 1e-30f * qn1;

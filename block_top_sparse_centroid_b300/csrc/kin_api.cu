@@ -33,13 +33,15 @@ kin_status cuda_fail(cudaError_t e, const char *what) {
 
 // Split planning is a pure function of the shapes (never of the device), so the
 // workspace size and the launch always agree.  The bf16 kernel runs one CTA per SM of a
-// B300 (148); the plan splits a row's kept list only when there are fewer rows than CTAs
-// (every split past the first costs a partial write and a merge), and aims at about three
-// score items per CTA.  Measured on the 32-sequence, 32K-context workload: one split per
-// row is 6 % faster than two.
+// B300 (148); the plan splits a row's kept list only when there are fewer than two rows
+// per CTA (every split past the first costs a partial write and a merge), and aims at
+// about three score items per CTA.  Measured: on the 256 rows of the 32-sequence,
+// 32K-context workload two splits per row are 4 % faster than one (rows finish their
+// selection at different times, and shorter attention items fill the gaps); 2 or 4 score
+// items per CTA instead of 3 change no workload by more than the run-to-run spread.
 constexpr int kPlanSMs = 148;
 #ifndef KIN_PLAN_ATTN_ITEMS
-#define KIN_PLAN_ATTN_ITEMS 1
+#define KIN_PLAN_ATTN_ITEMS 2
 #endif
 constexpr int kAttnItemsPerCta = KIN_PLAN_ATTN_ITEMS;
 constexpr int kScoreItemsPerCta = 3;

@@ -29,9 +29,6 @@ __device__ __forceinline__ void flag_error(int32_t *flag, int bits) {
 // --- bf16 <-> f32 -------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
-// The power of two at or below |x| for a normal x (its exponent alone); 0 for zero and
-// subnormal x.
-__device__ __forceinline__ float pow2_floor(float x) { return __uint_as_float(__float_as_uint(x) & 0x7f800000u); }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
